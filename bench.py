@@ -1,0 +1,422 @@
+"""Benchmark of the GB300 sliding-window SDPA backward.
+
+Default workload: gpt_oss-style sliding-window attention backward, b=2, h=16,
+d=64, S=8192, top-left causal with a 128-key left window, bf16, non-deterministic
+dQ (the configuration the cuDNN-frontend pages time on A100 at 0.980 ms).
+
+A step is one whole backward: preprocess, main, dq_convert, gqa_reduce (a
+no-op for MHA) -- every kernel of the path. The L2 cache is flushed (a 512 MB
+write) between timed steps, outside the per-step CUDA events.
+
+  value      attended TFLOP/s (10*d FLOPs per attended (q, k) pair per head)
+             with inputs resident in HBM, summed over ranks / max-over-ranks time
+  e2e        the same metric through the public API from pinned host buffers,
+             host->device copies of Q, K, V, O, dO, LSE and the device->host
+             read of dQ, dK, dV inside every timed step
+  roofline   the main kernel: algorithmic bytes per launch / its mean duration
+             (CUDA events on the launching stream) against measured HBM peak
+  cpu_baseline  the fp64 CPU oracle on the same workload (host cores)
+
+--impl reference times that oracle as the reference arm (no GPU work).
+Multi-GPU (torchrun): every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sliding_window_attention_sdpa_gb300 import inputs  # noqa: E402
+
+WORKLOADS = {
+    # name: (b, h_q, h_kv, s_q, s_kv, d, mask, window_left, dtype)
+    "gptoss_b2_h16_d64_w128_s2048": (2, 16, 16, 2048, 2048, 64, "tl", 128, "bf16"),
+    "gptoss_b2_h16_d64_w128_s4096": (2, 16, 16, 4096, 4096, 64, "tl", 128, "bf16"),
+    "gptoss_b2_h16_d64_w128_s8192": (2, 16, 16, 8192, 8192, 64, "tl", 128, "bf16"),
+    "gptoss_b2_h16_d64_w128_s32768": (2, 16, 16, 32768, 32768, 64, "tl", 128, "bf16"),
+    "gqa_b12_h48x6_d128_s16484_br_w96": (12, 48, 6, 16484, 16484, 128, "br", 96, "bf16"),
+    "gqa_b24_h28x4_d128_s128_br_w8000": (24, 28, 4, 128, 128, 128, "br", 8000, "f16"),
+    "nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000": (12, 40, 8, 128, 8960, 64, "br", 8000, "bf16"),
+    "winonly_b4_h16_d64_s4096_w512": (4, 16, 16, 4096, 4096, 64, "none", 512, "bf16"),
+}
+DEFAULT = "gptoss_b2_h16_d64_w128_s8192"
+MODE = {"none": 0, "tl": 1, "br": 2}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def attended_pairs(s_q: int, s_kv: int, mask: str, w: int) -> int:
+    """Attended (q, k) pairs per head in closed form: each row i reaches keys
+    j with anchor - w <= j (left window, if any) and j <= anchor (causal modes)."""
+    diag = s_kv - s_q if mask == "br" else 0
+    i = np.arange(s_q, dtype=np.int64)
+    anchor = i + diag
+    hi = np.minimum(anchor, s_kv - 1) if mask in ("tl", "br") else np.full(s_q, s_kv - 1)
+    lo = np.maximum(anchor - w, 0) if w >= 0 else np.zeros(s_q, np.int64)
+    return int(np.clip(hi - lo + 1, 0, None).sum())
+
+
+def algorithmic_bytes(b, h_q, h_kv, s_q, s_kv, d, gqa: bool):
+    """Main kernel, inputs read once and outputs written once: per q-row per
+    q-head Q, dO (2*2d B), LSE, D (8 B) and the fp32 dQ accumulation (4d B);
+    per kv-row per kv-head K, V (2*2d B) and dK, dV (2*2d B; fp32 partials
+    per q-head under GQA)."""
+    q_side = b * s_q * h_q * (2 * 2 * d + 8 + 4 * d)
+    kv_side = b * s_kv * h_kv * (2 * 2 * d) + (b * s_kv * h_q * 2 * 4 * d if gqa else b * s_kv * h_kv * 2 * 2 * d)
+    return q_side + kv_side
+
+
+class Problem:
+    """Device tensors, outputs, workspace and C-ABI params of one workload."""
+
+    def __init__(self, name: str, device, seed: int, deterministic: bool = False):
+        import sliding_window_attention_sdpa_gb300 as swa
+        self.swa = swa
+        b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+        self.name, self.b, self.h_q, self.h_kv, self.s_q, self.s_kv, self.d = name, b, hq, hkv, sq, skv, d
+        self.mask, self.w, self.dtype = mask, w, dt
+        self.scale = 1.0 / math.sqrt(d)
+        t = inputs.make_tensors((b, sq, hq, d), (b, skv, hkv, d), hq, dt, seed, False, device=device)
+        self.q, self.k, self.v, self.do = t.q, t.k, t.v, t.do
+        # O and LSE with the magnitudes of a real forward over ~(w+1) keys of
+        # N(0,1) logits: O ~ N(0, 1/n), LSE = log(n) + 1/2.
+        n = (w + 1) if w >= 0 else skv
+        n = min(n, skv)
+        self.o = (inputs.randn((b, sq, hq, d), seed * 16 + 6, torch.float32, device)
+                  / math.sqrt(n)).to(inputs.DTYPES[dt])
+        self.lse = torch.full((b, hq, sq), math.log(n) + 0.5, dtype=torch.float32, device=device)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.params = swa.make_params(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
+                                      self.dk, self.dv, scale=self.scale, mask_mode=MODE[mask],
+                                      window_left=w, deterministic=deterministic)
+        self.ws = swa.alloc_workspace(self.params, device)
+        self.flops = 10 * d * attended_pairs(sq, skv, mask, w) * b * hq
+        self.main_bytes = algorithmic_bytes(b, hq, hkv, sq, skv, d, hq != hkv)
+
+    def step(self, stream: int, ev=None):
+        """The whole backward; `ev` = (before_main, after_main) events."""
+        swa, p = self.swa, self.params
+        ws, nb = self.ws.data_ptr(), self.ws.numel()
+        swa._check(swa.sdpa_bwd_preprocess(p, ws, nb, stream), "preprocess")
+        if ev is not None:
+            ev[0].record()
+        swa._check(swa.sdpa_bwd(p, ws, nb, stream), "sdpa_bwd")
+        if ev is not None:
+            ev[1].record()
+        swa._check(swa.sdpa_bwd_dq_convert(p, ws, nb, stream), "dq_convert")
+        swa._check(swa.sdpa_bwd_gqa_reduce(p, ws, nb, stream), "gqa_reduce")
+
+    def launches_per_step(self) -> int:
+        return 3 + (1 if self.h_q != self.h_kv else 0)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return j["hbm_gbs"], j["bf16_tflops"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def time_device(prob: Problem, steps: int, warmup: int):
+    """Per-step device time (ms) of the whole backward and of the main kernel."""
+    stream = torch.cuda.current_stream()
+    sid = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=prob.q.device)
+    for _ in range(warmup):
+        prob.step(sid)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e in ev:
+        flush.fill_(1.0)
+        e[0].record()
+        prob.step(sid, (e[1], e[2]))
+        e[3].record()
+    torch.cuda.synchronize()
+    total = [a.elapsed_time(d) for a, _, _, d in ev]
+    main = [b.elapsed_time(c) for _, b, c, _ in ev]
+    return total, main
+
+
+def time_e2e(prob: Problem, steps: int, warmup: int):
+    """Same backward through the public API from pinned host buffers."""
+    import sliding_window_attention_sdpa_gb300 as swa
+    host_in = [t.cpu().pin_memory() for t in (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (prob.dq, prob.dk, prob.dv)]
+    dev_in = [torch.empty_like(t) for t in (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    kw = dict(scale=prob.scale, mask_mode=MODE[prob.mask], window_left=prob.w,
+              workspace=prob.ws)
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        dq, dk, dv, _ = swa.backward(*dev_in, **kw)
+        for h, d in zip(host_out, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def cpu_oracle_step(name: str, nthreads: int, units=None):
+    """One fp64 oracle backward (window-bounded sweep) of the workload on the
+    host cores; returns (seconds, fraction of the workload's units run)."""
+    import oracle
+    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+    t = inputs.make_tensors((b, sq, hq, d), (b, skv, hkv, d), hq, dt, 7, False)
+    f64 = lambda x: x.double().numpy()
+    n = min((w + 1) if w >= 0 else skv, skv)
+    o = (inputs.randn((b, sq, hq, d), 7 * 16 + 6) / math.sqrt(n)).to(inputs.DTYPES[dt])
+    lse = np.full((b, hq, sq), math.log(n) + 0.5)
+    p = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s_q=sq, s_kv=skv, d=d, scale=1 / math.sqrt(d),
+                       mask_mode=MODE[mask], window_left=w, nthreads=nthreads)
+    frac = 1.0
+    if units is not None and units < b * hkv:
+        m = np.zeros(b * hkv, np.uint8)
+        m[:units] = 1
+        p.unit_mask = m
+        frac = units / (b * hkv)
+    args = (f64(t.q), f64(t.k), f64(t.v), f64(o), f64(t.do), lse)
+    t0 = time.perf_counter()
+    oracle.backward(p, *args)
+    return time.perf_counter() - t0, frac
+
+
+def cpu_units_for_budget(name: str, budget_s: float, nthreads: int):
+    """Units (batch, kv-head) that fit about `budget_s` seconds of oracle time."""
+    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+    total = b * hkv
+    probe = max(1, min(total, nthreads))
+    t, frac = cpu_oracle_step(name, nthreads, probe)
+    per_unit_wave = t  # one wave of `probe` units in parallel
+    waves = max(1, int(budget_s / max(per_unit_wave, 1e-3)))
+    return min(total, probe * waves)
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference arm: K timed steps of the workload's
+    backward (bounded sample) on the host cores."""
+    if rank != 0:
+        return
+    name = args.workload
+    cores = os.cpu_count() or 1
+    units = cpu_units_for_budget(name, 20.0 / max(args.steps + args.warmup, 1), cores)
+    for _ in range(args.warmup):
+        cpu_oracle_step(name, cores, units)
+    times = []
+    frac = 1.0
+    for _ in range(args.steps):
+        t, frac = cpu_oracle_step(name, cores, units)
+        times.append(t)
+    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+    flops = 10 * d * attended_pairs(sq, skv, mask, w) * b * hq * frac
+    sec = statistics.mean(times)
+    val = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 / frac, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(name),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{units} of {b * hkv} (batch, kv-head) units per step, "
+                                   "time scaled to the whole workload"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "SWA bwd attended TFLOP/s (b2 h16 d64 W128 S8k bf16)"
+
+
+def workload_config(name):
+    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+    return {"workload": name, "global_batch": b, "seq_len": sq, "seq_len_kv": skv, "heads_q": hq,
+            "heads_kv": hkv, "head_dim": d, "mask": {"tl": "top_left_causal",
+                                                     "br": "bottom_right_causal",
+                                                     "none": "window_only"}[mask],
+            "window_left": w, "l2": "flushed (512 MB write) between timed steps",
+            "parallelism": "replicas"}
+
+
+def aggregate(per_rank_ms, per_rank_flops):
+    """Whole-job throughput: all ranks' FLOPs over the slowest rank's time."""
+    t = max(per_rank_ms)
+    return sum(per_rank_flops) / (t * 1e-3) / 1e12, t
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import sliding_window_attention_sdpa_gb300 as swa
+    swa.load()
+
+    prob = Problem(args.workload, dev, seed=1000 + 2, deterministic=args.deterministic)
+    peak_gbs, peak_tf, peak_kind = measured_peaks()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total, main_ms = time_device(prob, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    step_ms = sum(total) / len(total)
+    main_avg = sum(main_ms) / len(main_ms)
+    e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps // 2), 2)
+    status = swa.sdpa_bwd_check_status(prob.ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+    if dist is not None:
+        t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_max, e2e_max = t.tolist()
+    else:
+        step_max, e2e_max = step_ms, e2e_ms
+    value, _ = aggregate([step_max], [prob.flops * world])
+    e2e_val, _ = aggregate([e2e_max], [prob.flops * world])
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    achieved = prob.main_bytes / (main_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": prob.dtype, "data": "synthetic",
+        "config": workload_config(args.workload),
+        "main_kernel_ms": main_avg,
+        "main_kernel_tflops": prob.flops / (main_avg * 1e-3) / 1e12,
+        "tensor_peak_frac": prob.flops / (main_avg * 1e-3) / 1e12 / peak_tf,
+        "deterministic": bool(args.deterministic),
+        "device_status": int(status),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                     "frac": achieved / peak_gbs, "traffic": None,
+                     "kernel": "sdpa_bwd_main_kernel", "peak_kind": peak_kind,
+                     "algorithmic_bytes": prob.main_bytes},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_max,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": prob.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        name = args.workload
+        units = cpu_units_for_budget(name, 15.0, cores)
+        sec, frac = cpu_oracle_step(name, cores, units)
+        cpu_val = prob.flops * frac / sec / 1e12
+        b, hq, hkv = WORKLOADS[name][:3]
+        line["cpu_baseline"] = {"value": cpu_val, "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{units} of {b * hkv} (batch, kv-head) units, "
+                                          "fp64 window-bounded backward"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * sdpa_bwd.h -- C ABI of the GB300 (sm_103a) sliding-window scaled-dot-product
+ * attention backward: dQ, dK, dV and (with attention sinks) dSink.
+ *
+ * The operation (cuDNN-frontend PR #866 "frost(sdpa): bound the SM80 backward
+ * q-loop by the sliding window ... + window-aware deterministic relay",
+ * "Change" section; PR #557 "frost(sdpa): GQA/MQA, padding mask, right-band
+ * widening, and sink-token gradients for the SM120 f16 backward", "Summary"):
+ *
+ *   for batch b, q-head h, kv-head g = h / (h_q / h_kv), query row i < Lq_b:
+ *     anchor(i) = i + diag_b,  diag_b = Lkv_b - Lq_b (bottom-right) else 0
+ *     key j < Lkv_b is attended iff  anchor(i) - j <= window_left  (if >= 0)
+ *                                and j - anchor(i) <= right        (if >= 0)
+ *     where right = max(window_right, 0) for the causal modes and
+ *     window_right (negative = unbounded) for SDPA_MASK_NONE;
+ *     P_ij = exp(scale * q_i.k_j - LSE_i),  D_i = dO_i . O_i,
+ *     dS_ij = P_ij (dO_i.v_j - D_i),
+ *     dV_j = sum P_ij dO_i,  dK_j = scale sum dS_ij q_i,  dQ_i = scale sum dS_ij k_j,
+ *     dSink_h = -sum_{b, i < Lq_b} exp(sink_h - LSE_i) D_i.
+ *
+ * Each kv-tile's sweep over q-tiles is clamped on both sides by the window
+ * (work O(S*W) rather than O(S^2)); a kv-tile that no query reaches writes
+ * dK = dV = 0.
+ *
+ * Conventions common to every entry point:
+ *  - Ownership: the caller owns every buffer, including the workspace. The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Asynchrony: the four compute calls enqueue kernels on `stream` and return
+ *    without synchronising. They must be called in the order
+ *      sdpa_bwd_preprocess, sdpa_bwd, sdpa_bwd_dq_convert, sdpa_bwd_gqa_reduce
+ *    on one stream with the same params and workspace.
+ *  - Errors: argument checks run on the host before anything is enqueued and
+ *    return SDPA_ERR_INVALID_ARG / SDPA_ERR_UNSUPPORTED; sdpa_bwd_last_error()
+ *    then names the offending argument. A failed launch returns SDPA_ERR_CUDA.
+ *    Problems found on the device (a relay wait that ran out, sequence lengths
+ *    that do not fit their slots) are recorded in a status word inside the
+ *    workspace and reported by sdpa_bwd_check_status().
+ *  - Pointers marked (device) must be device memory of the current device.
+ */
+#ifndef SDPA_BWD_H
+#define SDPA_BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDPA_OK = 0,
+    SDPA_ERR_INVALID_ARG = 1,  /* bad shape, pointer, stride or flag */
+    SDPA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not 64/128) */
+    SDPA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    SDPA_ERR_TIMEOUT = 4,      /* a deterministic-relay wait ran out on the device */
+    SDPA_ERR_BAD_LENGTHS = 5,  /* device-side: a sequence length exceeds its slot */
+    SDPA_ERR_WORKSPACE = 6     /* workspace NULL, misaligned or too small */
+} sdpa_status_t;
+
+enum { SDPA_BF16 = 0, SDPA_F16 = 1 };
+enum { SDPA_BSHD = 0, SDPA_THD = 1 };
+enum { SDPA_MASK_NONE = 0, SDPA_MASK_TOP_LEFT = 1, SDPA_MASK_BOTTOM_RIGHT = 2 };
+
+/*
+ * Problem description. All strides are in elements; the feature (d) stride
+ * of every tensor is 1 and every other stride must be a multiple of 8
+ * elements (16 bytes), with 16-byte aligned base pointers.
+ *
+ * Layouts
+ *  SDPA_BSHD: Q, O, dO, dQ are [b, s_q, h_q, d]; K, V, dK, dV [b, s_kv, h_kv, d]
+ *    (strides[0] = batch, [1] = sequence, [2] = head). seq_q_lens/seq_kv_lens
+ *    (device int32 [b], optional) give the actual lengths (padding mask); NULL
+ *    means every sequence is full (s_q / s_kv). LSE is fp32 [b, h_q, s_q],
+ *    contiguous.
+ *  SDPA_THD: tokens of all sequences packed: Q, O, dO, dQ are [total_q, h_q, d],
+ *    K, V, dK, dV [total_kv, h_kv, d] (strides[0] ignored, [1] = token,
+ *    [2] = head). q_offsets/kv_offsets (device int32 [b+1], required) are the
+ *    first token of each sequence's slot, with offsets[0] = 0 and
+ *    offsets[b] = total. Lengths (optional, device int32 [b]) may be shorter
+ *    than the slots; tokens of a slot past its length are "gap" tokens. s_q and
+ *    s_kv must be at least the longest slot (offsets difference). LSE is fp32
+ *    [h_q, total_q], contiguous.
+ *  Rows and tokens past a sequence's length receive dQ = 0 / dK = dV = 0; their
+ *  input values are never read into a result.
+ *
+ * Semantics of the mask fields are those given at the top of this file.
+ * LSE is the natural-log normaliser of the forward, including the sink
+ * logit when a sink is used; a row that attended nothing has LSE = -inf.
+ */
+typedef struct sdpa_bwd_params {
+    int32_t dtype;          /* SDPA_BF16 | SDPA_F16 for Q, K, V, O, dO, dQ, dK, dV */
+    int32_t layout;         /* SDPA_BSHD | SDPA_THD */
+    int32_t mask_mode;      /* SDPA_MASK_* */
+    int32_t deterministic;  /* 0: dQ by unordered fp32 atomics; 1: ordered relay,
+                               bitwise repeatable results */
+    int64_t b;              /* batch size (THD: number of sequences) */
+    int64_t h_q, h_kv;      /* heads; h_q % h_kv == 0 (MHA, GQA, MQA) */
+    int64_t s_q, s_kv;      /* BSHD: padded lengths; THD: longest slot */
+    int64_t total_q, total_kv; /* THD: tokens in the packed tensors; BSHD: unused */
+    int64_t d;              /* head dimension: 64 or 128 */
+    int64_t window_left;    /* < 0: no left window */
+    int64_t window_right;   /* right band; see the top of this file */
+    float scale;            /* softmax scale applied to q.k (e.g. 1/sqrt(d)) */
+    int32_t reserved0;
+    const int32_t *seq_q_lens, *seq_kv_lens; /* device [b] or NULL */
+    const int32_t *q_offsets, *kv_offsets;   /* device [b+1], THD only */
+    const void *q, *k, *v, *o, *dout;        /* device, dtype */
+    const float *lse;                        /* device fp32 (layout above) */
+    const float *sink;                       /* device fp32 [h_q] or NULL */
+    void *dq, *dk, *dv;                      /* device outputs, dtype */
+    float *dsink;                            /* device fp32 [h_q]; set iff sink */
+    int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3], do_stride[3];
+    int64_t dq_stride[3], dk_stride[3], dv_stride[3];
+} sdpa_bwd_params;
+
+/*
+ * Workspace size in bytes for `params` (0 on invalid params; see
+ * sdpa_bwd_last_error). The workspace holds the fp32 dQ accumulator, D = rowsum
+ * (dO*O), the relay counters, the per-q-head fp32 dK/dV partials when
+ * h_q != h_kv, the dSink partials and the status word. It must be 256-byte
+ * aligned device memory; its contents need no initialisation.
+ */
+size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params *params);
+
+/*
+ * Preprocess ("dot" kernel of PR #557's four-kernel split; delta of its dSink
+ * formula): D[b,h,i] = sum_d dO*O in fp32 for every row, zeroes the fp32 dQ
+ * accumulator, the relay counters and the status word, and writes the dSink
+ * partials -exp(sink_h - LSE_i) * D_i summed over each block of unpadded rows.
+ */
+sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params *params, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * Main backward ("main" kernel; PR #866 clamp and relay): one CTA per
+ * (kv-tile, q-head, batch). Recomputes P and dS for each q-tile in the
+ * clamped range [q_lo, q_hi) and accumulates dV, dK in tensor memory; adds
+ * scale * dS K into the fp32 dQ accumulator (atomics, or in deterministic mode
+ * the relay whose turn counts from kv_first = max((q_row0 + diag - W) //
+ * tile_kv, 0)); stores dK, dV (h_q == h_kv) or fp32 per-q-head partials.
+ */
+sdpa_status_t sdpa_bwd(const sdpa_bwd_params *params, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/*
+ * dQ convert ("cvt" kernel): dQ = dtype(fp32 accumulator), zero on padded rows,
+ * and dsink[h] = fixed-order sum of the dSink partials (when a sink is used).
+ */
+sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params *params, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * GQA reduction ("reduce" kernel, PR #557 GQA/MQA): dK[., g] and dV[., g] are
+ * the sums over the q-heads of group g of the per-q-head partials, in head
+ * order. Returns SDPA_OK without enqueuing anything when h_q == h_kv.
+ */
+sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream` and returns the device status word of the last
+ * backward run on `workspace`: SDPA_OK, SDPA_ERR_TIMEOUT (a relay wait gave up;
+ * dQ is then incomplete) or SDPA_ERR_BAD_LENGTHS.
+ */
+sdpa_status_t sdpa_bwd_check_status(const void *workspace, void *stream);
+
+/* Message of the last host-side error on the calling thread ("" if none). */
+const char *sdpa_bwd_last_error(void);
+
+/* sizeof(sdpa_bwd_params) as compiled into the library, for binding checks. */
+size_t sdpa_bwd_params_bytes(void);
+
+/* Main-kernel tile sizes (rows of a kv-tile and of a q-tile). */
+int32_t sdpa_bwd_tile_kv(void);
+int32_t sdpa_bwd_tile_q(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_BWD_H */

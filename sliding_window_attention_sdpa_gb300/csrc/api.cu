@@ -1,0 +1,352 @@
+// api.cu -- the C ABI declared in include/sdpa_bwd.h: host-side argument
+// checks, the workspace layout, and the launches of the four kernels on the
+// caller's stream. Nothing here allocates or synchronises (except
+// sdpa_bwd_check_status, which reads the device status word).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/sdpa_bwd.h"
+#include "sdpa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sdpa_status_t fail(sdpa_status_t code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side validation that needs no device access.
+sdpa_status_t check_shape(const sdpa_bwd_params* p)
+{
+    if (p == nullptr) return fail(SDPA_ERR_INVALID_ARG, "params is NULL");
+    if (p->dtype != SDPA_BF16 && p->dtype != SDPA_F16)
+        return fail(SDPA_ERR_INVALID_ARG, "dtype: expected SDPA_BF16 or SDPA_F16, got %d", p->dtype);
+    if (p->layout != SDPA_BSHD && p->layout != SDPA_THD)
+        return fail(SDPA_ERR_INVALID_ARG, "layout: expected SDPA_BSHD or SDPA_THD, got %d", p->layout);
+    if (p->mask_mode < SDPA_MASK_NONE || p->mask_mode > SDPA_MASK_BOTTOM_RIGHT)
+        return fail(SDPA_ERR_INVALID_ARG, "mask_mode: unknown value %d", p->mask_mode);
+    if (p->deterministic != 0 && p->deterministic != 1)
+        return fail(SDPA_ERR_INVALID_ARG, "deterministic: expected 0 or 1, got %d", p->deterministic);
+    if (p->b < 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s_q < 0 || p->s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG,
+                    "shape: b=%lld h_q=%lld h_kv=%lld s_q=%lld s_kv=%lld (need b,s >= 0, h > 0)",
+                    (long long)p->b, (long long)p->h_q, (long long)p->h_kv, (long long)p->s_q,
+                    (long long)p->s_kv);
+    if (p->h_q % p->h_kv != 0)
+        return fail(SDPA_ERR_INVALID_ARG, "h_q=%lld is not a multiple of h_kv=%lld",
+                    (long long)p->h_q, (long long)p->h_kv);
+    if (p->d != 64 && p->d != 128)
+        return fail(SDPA_ERR_UNSUPPORTED, "d=%lld: only head dimensions 64 and 128 are implemented",
+                    (long long)p->d);
+    if (p->window_left < -1 || p->window_right < -1)
+        return fail(SDPA_ERR_INVALID_ARG, "window_left=%lld window_right=%lld: must be >= -1",
+                    (long long)p->window_left, (long long)p->window_right);
+    if (!(p->scale > 0.f) || p->scale != p->scale)
+        return fail(SDPA_ERR_INVALID_ARG, "scale must be a positive finite number");
+    if (p->layout == SDPA_THD) {
+        if (p->q_offsets == nullptr || p->kv_offsets == nullptr)
+            return fail(SDPA_ERR_INVALID_ARG, "THD layout needs q_offsets and kv_offsets");
+        if (p->total_q < 0 || p->total_kv < 0)
+            return fail(SDPA_ERR_INVALID_ARG, "THD layout: total_q/total_kv must be >= 0");
+    }
+    if (p->layout == SDPA_BSHD && p->mask_mode == SDPA_MASK_BOTTOM_RIGHT &&
+        p->seq_q_lens == nullptr && p->seq_kv_lens == nullptr && p->s_q > p->s_kv)
+        return fail(SDPA_ERR_UNSUPPORTED,
+                    "bottom-right causal with s_q=%lld > s_kv=%lld is not supported",
+                    (long long)p->s_q, (long long)p->s_kv);
+    if ((p->sink == nullptr) != (p->dsink == nullptr))
+        return fail(SDPA_ERR_INVALID_ARG, "sink and dsink must both be set or both be NULL");
+    return SDPA_OK;
+}
+
+sdpa_status_t check_strides(const char* name, const int64_t* st, bool thd)
+{
+    for (int i = thd ? 1 : 0; i < 3; ++i)
+        if (st[i] < 0 || st[i] % 8 != 0)
+            return fail(SDPA_ERR_INVALID_ARG,
+                        "%s_stride[%d]=%lld: strides must be non-negative multiples of 8 elements",
+                        name, i, (long long)st[i]);
+    return SDPA_OK;
+}
+
+sdpa_status_t check_device_ptr(const char* name, const void* ptr, bool required, int device)
+{
+    if (ptr == nullptr) {
+        if (required) return fail(SDPA_ERR_INVALID_ARG, "%s is NULL", name);
+        return SDPA_OK;
+    }
+    if (!aligned16(ptr))
+        return fail(SDPA_ERR_INVALID_ARG, "%s=%p is not 16-byte aligned", name, ptr);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDPA_ERR_INVALID_ARG, "%s=%p: not a CUDA pointer (%s)", name, ptr,
+                    cudaGetErrorString(e));
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(SDPA_ERR_INVALID_ARG, "%s=%p is not device memory (memory type %d)", name, ptr,
+                    (int)attr.type);
+    if (attr.device != device)
+        return fail(SDPA_ERR_INVALID_ARG, "%s=%p lives on device %d, current device is %d", name, ptr,
+                    attr.device, device);
+    return SDPA_OK;
+}
+
+int64_t rows_q(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_q : p->b * p->s_q; }
+int64_t rows_kv(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_kv : p->b * p->s_kv; }
+
+swa::WsLayout layout_of(const sdpa_bwd_params* p)
+{
+    swa::WsLayout w{};
+    const int64_t rq = rows_q(p), rkv = rows_kv(p);
+    const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
+    w.n_sems = p->b * p->h_q * nqt;
+    w.n_row_blocks = (rq + swa::kPreRows - 1) / swa::kPreRows;
+    size_t off = 0;
+    w.status = off;
+    off = align256(off + 16);
+    w.dq_acc = off;
+    off = align256(off + static_cast<size_t>(rq) * p->h_q * p->d * 4);
+    w.delta = off;
+    off = align256(off + static_cast<size_t>(rq) * p->h_q * 4);
+    w.sems = off;
+    off = align256(off + static_cast<size_t>(w.n_sems) * 4);
+    w.dsink_part = off;
+    if (p->sink != nullptr) off = align256(off + static_cast<size_t>(p->h_q) * w.n_row_blocks * 4);
+    w.dk_ws = w.dv_ws = off;
+    if (p->h_q != p->h_kv) {
+        const size_t part = static_cast<size_t>(rkv) * p->h_q * p->d * 4;
+        w.dk_ws = off;
+        off = align256(off + part);
+        w.dv_ws = off;
+        off = align256(off + part);
+    }
+    w.total = off;
+    return w;
+}
+
+swa::Geometry geometry_of(const sdpa_bwd_params* p)
+{
+    swa::Geometry g{};
+    g.layout = p->layout;
+    g.mask_mode = p->mask_mode;
+    g.b = p->b;
+    g.h_q = p->h_q;
+    g.h_kv = p->h_kv;
+    g.s_q = p->s_q;
+    g.s_kv = p->s_kv;
+    g.d = p->d;
+    g.rows_q = rows_q(p);
+    g.rows_kv = rows_kv(p);
+    g.window_left = p->window_left;
+    if (p->mask_mode == SDPA_MASK_NONE) g.right = p->window_right;
+    else g.right = p->window_right > 0 ? p->window_right : 0;
+    g.seq_q_lens = p->seq_q_lens;
+    g.seq_kv_lens = p->seq_kv_lens;
+    g.q_offsets = p->q_offsets;
+    g.kv_offsets = p->kv_offsets;
+    return g;
+}
+
+// Full check before a launch: shapes, strides, pointers and workspace.
+sdpa_status_t check_all(const sdpa_bwd_params* p, const void* ws, size_t ws_bytes)
+{
+    sdpa_status_t st = check_shape(p);
+    if (st != SDPA_OK) return st;
+    const bool thd = p->layout == SDPA_THD;
+    const struct { const char* n; const int64_t* s; } strides[] = {
+        {"q", p->q_stride},   {"k", p->k_stride},   {"v", p->v_stride},   {"o", p->o_stride},
+        {"dout", p->do_stride}, {"dq", p->dq_stride}, {"dk", p->dk_stride}, {"dv", p->dv_stride}};
+    for (const auto& s : strides)
+        if ((st = check_strides(s.n, s.s, thd)) != SDPA_OK) return st;
+    const swa::WsLayout w = layout_of(p);
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(SDPA_ERR_WORKSPACE, "workspace=%p must be non-NULL and 256-byte aligned", ws);
+    if (ws_bytes < w.total)
+        return fail(SDPA_ERR_WORKSPACE, "workspace_bytes=%zu, need %zu", ws_bytes, w.total);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDPA_ERR_CUDA, "no CUDA device available");
+    }
+    const bool empty_q = rows_q(p) == 0, empty_kv = rows_kv(p) == 0;
+    const struct { const char* n; const void* ptr; bool req; } ptrs[] = {
+        {"q", p->q, !empty_q},       {"k", p->k, !empty_kv},     {"v", p->v, !empty_kv},
+        {"o", p->o, !empty_q},       {"dout", p->dout, !empty_q}, {"lse", p->lse, !empty_q},
+        {"dq", p->dq, !empty_q},     {"dk", p->dk, !empty_kv},   {"dv", p->dv, !empty_kv},
+        {"sink", p->sink, false},    {"dsink", p->dsink, false},
+        {"seq_q_lens", p->seq_q_lens, false}, {"seq_kv_lens", p->seq_kv_lens, false},
+        {"q_offsets", p->q_offsets, thd}, {"kv_offsets", p->kv_offsets, thd},
+        {"workspace", ws, true}};
+    for (const auto& q : ptrs)
+        if ((st = check_device_ptr(q.n, q.ptr, q.req, dev)) != SDPA_OK) return st;
+    return SDPA_OK;
+}
+
+sdpa_status_t cuda_status(cudaError_t e, const char* what)
+{
+    if (e == cudaSuccess) return SDPA_OK;
+    return fail(SDPA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+void copy3(int64_t* dst, const int64_t* src) { memcpy(dst, src, 3 * sizeof(int64_t)); }
+
+}  // namespace
+
+extern "C" {
+
+size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params* p)
+{
+    if (check_shape(p) != SDPA_OK) return 0;
+    g_last_error.clear();
+    return layout_of(p).total;
+}
+
+sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void* stream)
+{
+    sdpa_status_t st = check_all(p, ws, ws_bytes);
+    if (st != SDPA_OK) return st;
+    const swa::WsLayout w = layout_of(p);
+    swa::PreArgs a{};
+    a.g = geometry_of(p);
+    a.o = p->o;
+    a.dout = p->dout;
+    a.lse = p->lse;
+    a.sink = p->sink;
+    copy3(a.o_stride, p->o_stride);
+    copy3(a.do_stride, p->do_stride);
+    a.dq_acc = at<float>(ws, w.dq_acc);
+    a.delta = at<float>(ws, w.delta);
+    a.status = at<int32_t>(ws, w.status);
+    a.sems = at<int32_t>(ws, w.sems);
+    a.n_sems = w.n_sems;
+    a.dsink_part = p->sink ? at<float>(ws, w.dsink_part) : nullptr;
+    a.n_row_blocks = w.n_row_blocks;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a.n_row_blocks == 0) {
+        // nothing to reduce: still reset status, ticket and the dSink output
+        st = cuda_status(cudaMemsetAsync(a.status, 0, 8, s), "preprocess memset");
+        if (st == SDPA_OK && p->dsink)
+            st = cuda_status(cudaMemsetAsync(p->dsink, 0, p->h_q * sizeof(float), s), "dsink memset");
+        return st;
+    }
+    return cuda_status(swa::launch_preprocess(a, p->dtype, s), "preprocess launch");
+}
+
+sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void* stream)
+{
+    sdpa_status_t st = check_all(p, ws, ws_bytes);
+    if (st != SDPA_OK) return st;
+    const swa::WsLayout w = layout_of(p);
+    swa::MainArgs a{};
+    a.g = geometry_of(p);
+    a.q = p->q;
+    a.k = p->k;
+    a.v = p->v;
+    a.dout = p->dout;
+    a.lse = p->lse;
+    a.delta = at<float>(ws, w.delta);
+    a.dq_acc = at<float>(ws, w.dq_acc);
+    a.dk = p->dk;
+    a.dv = p->dv;
+    if (p->h_q != p->h_kv) {
+        a.dk_ws = at<float>(ws, w.dk_ws);
+        a.dv_ws = at<float>(ws, w.dv_ws);
+    }
+    a.status = at<int32_t>(ws, w.status);
+    a.sems = at<int32_t>(ws, w.sems);
+    copy3(a.q_stride, p->q_stride);
+    copy3(a.k_stride, p->k_stride);
+    copy3(a.v_stride, p->v_stride);
+    copy3(a.do_stride, p->do_stride);
+    copy3(a.dk_stride, p->dk_stride);
+    copy3(a.dv_stride, p->dv_stride);
+    a.n_kv_tiles = (p->s_kv + swa::kTileKV - 1) / swa::kTileKV;
+    a.n_q_tiles = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
+    a.scale = p->scale;
+    a.scale_log2 = p->scale * 1.4426950408889634f;
+    a.deterministic = p->deterministic;
+    a.timeout_ns = 2000000000LL;
+    return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
+}
+
+sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void* stream)
+{
+    sdpa_status_t st = check_all(p, ws, ws_bytes);
+    if (st != SDPA_OK) return st;
+    const swa::WsLayout w = layout_of(p);
+    swa::CvtArgs a{};
+    a.g = geometry_of(p);
+    a.dq_acc = at<float>(ws, w.dq_acc);
+    a.dq = p->dq;
+    copy3(a.dq_stride, p->dq_stride);
+    a.dsink_part = p->sink ? at<float>(ws, w.dsink_part) : nullptr;
+    a.n_row_blocks = w.n_row_blocks;
+    a.dsink = p->dsink;
+    if (a.n_row_blocks == 0) return SDPA_OK;
+    return cuda_status(swa::launch_dq_convert(a, p->dtype, static_cast<cudaStream_t>(stream)),
+                       "dq_convert launch");
+}
+
+sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void* stream)
+{
+    sdpa_status_t st = check_all(p, ws, ws_bytes);
+    if (st != SDPA_OK) return st;
+    if (p->h_q == p->h_kv) return SDPA_OK;
+    const swa::WsLayout w = layout_of(p);
+    swa::ReduceArgs a{};
+    a.g = geometry_of(p);
+    a.dk_ws = at<float>(ws, w.dk_ws);
+    a.dv_ws = at<float>(ws, w.dv_ws);
+    a.dk = p->dk;
+    a.dv = p->dv;
+    copy3(a.dk_stride, p->dk_stride);
+    copy3(a.dv_stride, p->dv_stride);
+    return cuda_status(swa::launch_gqa_reduce(a, p->dtype, static_cast<cudaStream_t>(stream)),
+                       "gqa_reduce launch");
+}
+
+sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
+{
+    if (ws == nullptr) return fail(SDPA_ERR_WORKSPACE, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t host[2] = {0, 0};
+    sdpa_status_t st = cuda_status(cudaStreamSynchronize(s), "stream synchronize");
+    if (st != SDPA_OK) return st;
+    st = cuda_status(cudaMemcpy(host, ws, sizeof(host), cudaMemcpyDeviceToHost), "status read");
+    if (st != SDPA_OK) return st;
+    if (host[0] == SDPA_ERR_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a relay or MMA wait ran out on the device");
+    if (host[0] == SDPA_ERR_BAD_LENGTHS)
+        return fail(SDPA_ERR_BAD_LENGTHS, "a sequence length exceeds its slot (or s_q/s_kv)");
+    if (host[0] != 0) return fail(SDPA_ERR_CUDA, "unknown device status %d", host[0]);
+    return SDPA_OK;
+}
+
+const char* sdpa_bwd_last_error(void) { return g_last_error.c_str(); }
+
+size_t sdpa_bwd_params_bytes(void) { return sizeof(sdpa_bwd_params); }
+
+int32_t sdpa_bwd_tile_kv(void) { return swa::kTileKV; }
+int32_t sdpa_bwd_tile_q(void) { return swa::kTileQ; }
+
+}  // extern "C"

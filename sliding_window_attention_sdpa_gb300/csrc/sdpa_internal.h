@@ -1,0 +1,104 @@
+// sdpa_internal.h -- argument blocks shared by the host launcher (api.cu) and
+// the kernels (aux_kernels.cu, main_kernel.cu). Plain structs passed by value
+// as kernel parameters.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace swa {
+
+constexpr int kTileKV = 128;      // kv rows per CTA work item (MMA M of dK/dV side)
+constexpr int kTileQ = 128;       // q rows per inner-loop step
+constexpr int kPreRows = 64;      // token rows per preprocess CTA
+constexpr int kStatusTimeout = 4; // same codes as sdpa_status_t
+constexpr int kStatusBadLengths = 5;
+
+// Workspace layout (byte offsets from the workspace base, 256-B aligned).
+struct WsLayout {
+    size_t status;      // int32 status, int32 ticket counter
+    size_t dq_acc;      // fp32 [rows_q][h_q][d]
+    size_t delta;       // fp32, indexed like LSE
+    size_t sems;        // int32 [b][h_q][n_q_tiles]
+    size_t dsink_part;  // fp32 [h_q][n_row_blocks]
+    size_t dk_ws;       // fp32 [rows_kv][h_q][d]  (GQA only)
+    size_t dv_ws;       // fp32 [rows_kv][h_q][d]  (GQA only)
+    size_t total;
+    int64_t n_sems;
+    int64_t n_row_blocks;
+};
+
+// Sequence geometry common to all kernels.
+struct Geometry {
+    int32_t layout;     // 0 BSHD, 1 THD
+    int32_t mask_mode;  // 0 none, 1 top-left, 2 bottom-right
+    int64_t b, h_q, h_kv, s_q, s_kv, d;
+    int64_t rows_q, rows_kv;   // BSHD: b*s; THD: total tokens
+    int64_t window_left;       // < 0 unbounded
+    int64_t right;             // effective right bound, < 0 unbounded
+    const int32_t* seq_q_lens;
+    const int32_t* seq_kv_lens;
+    const int32_t* q_offsets;
+    const int32_t* kv_offsets;
+};
+
+struct PreArgs {
+    Geometry g;
+    const void* o;
+    const void* dout;
+    const float* lse;
+    const float* sink;
+    int64_t o_stride[3], do_stride[3];
+    float* dq_acc;
+    float* delta;
+    int32_t* status;     // status + ticket (2 ints)
+    int32_t* sems;
+    int64_t n_sems;
+    float* dsink_part;
+    int64_t n_row_blocks;
+};
+
+struct MainArgs {
+    Geometry g;
+    const void *q, *k, *v, *dout;
+    const float* lse;
+    const float* delta;
+    float* dq_acc;
+    void *dk, *dv;
+    float *dk_ws, *dv_ws;     // non-null: GQA partial output
+    int32_t* status;
+    int32_t* sems;
+    int64_t q_stride[3], k_stride[3], v_stride[3], do_stride[3], dk_stride[3], dv_stride[3];
+    int64_t n_kv_tiles;       // tiles per sequence slot (grid x)
+    int64_t n_q_tiles;        // relay counters per (b, h)
+    float scale;
+    float scale_log2;         // scale * log2(e)
+    int32_t deterministic;
+    int64_t timeout_ns;
+};
+
+struct CvtArgs {
+    Geometry g;
+    const float* dq_acc;
+    void* dq;
+    int64_t dq_stride[3];
+    const float* dsink_part;
+    int64_t n_row_blocks;
+    float* dsink;
+};
+
+struct ReduceArgs {
+    Geometry g;
+    const float *dk_ws, *dv_ws;
+    void *dk, *dv;
+    int64_t dk_stride[3], dv_stride[3];
+};
+
+// Launchers (defined next to their kernels). Return the launch error.
+cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_gqa_reduce(const ReduceArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_main(const MainArgs& a, int dtype, cudaStream_t s);
+
+}  // namespace swa

@@ -1,0 +1,78 @@
+// seq.cuh -- per-sequence geometry on the device: where a sequence's rows
+// live (BSHD batch slot or THD token slot), its actual lengths, and the
+// bottom-right diagonal shift. Lengths larger than the slot are clamped to it
+// and reported through the status word.
+#pragma once
+
+#include "sdpa_internal.h"
+
+namespace swa {
+
+struct SeqInfo {
+    int64_t q_row0, kv_row0;   // first row of the slot in the packed row space
+    int64_t slot_q, slot_kv;   // rows in the slot
+    int64_t len_q, len_kv;     // actual lengths (<= slot)
+    int64_t diag;              // anchor(i) = i + diag
+    bool bad;                  // a length exceeded its slot (clamped)
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const Geometry& g, int64_t bi)
+{
+    SeqInfo s;
+    if (g.layout == 1) {
+        s.q_row0 = g.q_offsets[bi];
+        s.kv_row0 = g.kv_offsets[bi];
+        s.slot_q = g.q_offsets[bi + 1] - s.q_row0;
+        s.slot_kv = g.kv_offsets[bi + 1] - s.kv_row0;
+    } else {
+        s.q_row0 = bi * g.s_q;
+        s.kv_row0 = bi * g.s_kv;
+        s.slot_q = g.s_q;
+        s.slot_kv = g.s_kv;
+    }
+    s.len_q = g.seq_q_lens ? g.seq_q_lens[bi] : s.slot_q;
+    s.len_kv = g.seq_kv_lens ? g.seq_kv_lens[bi] : s.slot_kv;
+    s.bad = s.len_q < 0 || s.len_kv < 0 || s.len_q > s.slot_q || s.len_kv > s.slot_kv ||
+            s.slot_q < 0 || s.slot_kv < 0 || s.slot_q > g.s_q || s.slot_kv > g.s_kv;
+    s.len_q = s.len_q < 0 ? 0 : (s.len_q > s.slot_q ? s.slot_q : s.len_q);
+    s.len_kv = s.len_kv < 0 ? 0 : (s.len_kv > s.slot_kv ? s.slot_kv : s.len_kv);
+    s.diag = g.mask_mode == 2 ? s.len_kv - s.len_q : 0;
+    return s;
+}
+
+// Sequence holding packed q row `row` (THD: largest bi with offsets[bi] <= row).
+__device__ __forceinline__ int64_t q_row_seq(const Geometry& g, int64_t row)
+{
+    if (g.layout != 1) return row / g.s_q;
+    int64_t lo = 0, hi = g.b;
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (g.q_offsets[mid] <= row) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Element offset of (packed row, head) for a tensor with strides
+// (batch, sequence/token, head); BSHD rows are split back into (bi, i).
+__device__ __forceinline__ int64_t elem_offset(const Geometry& g, const int64_t* st, int64_t row,
+                                               int64_t seq_len_max, int64_t head)
+{
+    if (g.layout == 1) return row * st[1] + head * st[2];
+    const int64_t bi = row / seq_len_max, i = row - bi * seq_len_max;
+    return bi * st[0] + i * st[1] + head * st[2];
+}
+
+// Index of the per-row statistic (LSE, D) of q-head h at packed q row `row`.
+__device__ __forceinline__ int64_t stat_offset(const Geometry& g, int64_t row, int64_t h)
+{
+    if (g.layout == 1) return h * g.rows_q + row;
+    const int64_t bi = row / g.s_q, i = row - bi * g.s_q;
+    return (bi * g.h_q + h) * g.s_q + i;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+}  // namespace swa

@@ -33,20 +33,23 @@ class Tensors:
     sink: Optional[torch.Tensor]
 
 
-def randn(shape, seed: int, dtype=torch.float32) -> torch.Tensor:
-    g = torch.Generator().manual_seed(int(seed))
-    return torch.randn(*shape, generator=g, dtype=torch.float32).to(dtype)
+def randn(shape, seed: int, dtype=torch.float32, device="cpu") -> torch.Tensor:
+    """N(0, 1) drawn in fp32 by torch's generator on `device`, then cast (RNE).
+    A CPU and a CUDA draw with the same seed differ; each workload uses one."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=device).to(dtype)
 
 
-def make_tensors(q_shape, kv_shape, h_q: int, dtype: str, seed: int, sink: bool) -> Tensors:
-    """Q, K, V, dO (I/O dtype, CPU) and optional fp32 sink logits."""
+def make_tensors(q_shape, kv_shape, h_q: int, dtype: str, seed: int, sink: bool,
+                 device="cpu") -> Tensors:
+    """Q, K, V, dO (I/O dtype) and optional fp32 sink logits on `device`."""
     dt = DTYPES[dtype]
     return Tensors(
-        q=randn(q_shape, seed * 16 + 1, dt),
-        k=randn(kv_shape, seed * 16 + 2, dt),
-        v=randn(kv_shape, seed * 16 + 3, dt),
-        do=randn(q_shape, seed * 16 + 4, dt),
-        sink=randn((h_q,), seed * 16 + 5) if sink else None,
+        q=randn(q_shape, seed * 16 + 1, dt, device),
+        k=randn(kv_shape, seed * 16 + 2, dt, device),
+        v=randn(kv_shape, seed * 16 + 3, dt, device),
+        do=randn(q_shape, seed * 16 + 4, dt, device),
+        sink=randn((h_q,), seed * 16 + 5, torch.float32, device) if sink else None,
     )
 
 

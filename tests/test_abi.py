@@ -1,0 +1,110 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports every
+entry point declared in include/*.h, and rejects bad arguments on the host
+with a message naming the argument (no GPU needed: validation runs before any
+device access)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import sliding_window_attention_sdpa_gb300 as swa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    swa._build.build()
+    return swa.load()
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(sdpa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "sdpa_bwd" in names and "sdpa_bwd_preprocess" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(swa.ENTRY_POINTS) | {"sdpa_bwd_no_alloc"}
+
+
+def test_params_struct_matches_binding(lib):
+    assert lib.sdpa_bwd_params_bytes() == ctypes.sizeof(swa.SdpaBwdParams)
+    assert lib.sdpa_bwd_tile_kv() == 128 and lib.sdpa_bwd_tile_q() == 128
+
+
+def base_params(**kw):
+    p = swa.SdpaBwdParams()
+    p.dtype, p.layout, p.mask_mode = swa.SDPA_BF16, swa.SDPA_BSHD, swa.SDPA_MASK_TOP_LEFT
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 2, 4, 4, 256, 256, 64
+    p.window_left, p.window_right, p.scale = 32, -1, 0.125
+    st = swa._i64x3(256 * 4 * 64, 4 * 64, 64)
+    for f in ("q", "k", "v", "o", "dout", "dq", "dk", "dv"):
+        setattr(p, f + "_stride" if f != "dout" else "do_stride", st)
+        setattr(p, f, 4096)
+    p.lse = 4096
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_workspace_bytes():
+    p = base_params()
+    n = swa.sdpa_bwd_workspace_bytes(p)
+    # dQ accumulator alone is b*s*h*d*4 bytes
+    assert n >= 2 * 256 * 4 * 64 * 4
+    g = base_params(h_kv=2)
+    assert swa.sdpa_bwd_workspace_bytes(g) >= n + 2 * (2 * 256 * 4 * 64 * 4)
+    assert swa.sdpa_bwd_workspace_bytes(base_params(d=96)) == 0
+    assert "d=96" in swa.last_error()
+
+
+@pytest.mark.parametrize("field,value,code,needle", [
+    ("dtype", 7, swa.SDPA_ERR_INVALID_ARG, "dtype"),
+    ("layout", 3, swa.SDPA_ERR_INVALID_ARG, "layout"),
+    ("mask_mode", 9, swa.SDPA_ERR_INVALID_ARG, "mask_mode"),
+    ("h_kv", 3, swa.SDPA_ERR_INVALID_ARG, "multiple of h_kv"),
+    ("d", 80, swa.SDPA_ERR_UNSUPPORTED, "d=80"),
+    ("window_left", -5, swa.SDPA_ERR_INVALID_ARG, "window_left"),
+    ("deterministic", 2, swa.SDPA_ERR_INVALID_ARG, "deterministic"),
+    ("sink", 4096, swa.SDPA_ERR_INVALID_ARG, "dsink"),
+    ("scale", 0.0, swa.SDPA_ERR_INVALID_ARG, "scale"),
+])
+def test_host_validation(field, value, code, needle):
+    p = base_params(**{field: value})
+    for fn in (swa.sdpa_bwd_preprocess, swa.sdpa_bwd, swa.sdpa_bwd_dq_convert,
+               swa.sdpa_bwd_gqa_reduce):
+        assert fn(p, 0, 0, None) == code
+        assert needle in swa.last_error()
+
+
+def test_bad_stride_and_workspace():
+    p = base_params()
+    p.k_stride = swa._i64x3(256 * 4 * 64, 4 * 64 + 3, 64)
+    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_INVALID_ARG
+    assert "k_stride[1]" in swa.last_error()
+    p = base_params()
+    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_WORKSPACE
+    assert swa.sdpa_bwd(p, 256, 16, None) == swa.SDPA_ERR_WORKSPACE
+    assert "need" in swa.last_error()
+
+
+def test_bottom_right_with_longer_queries_is_rejected():
+    p = base_params(mask_mode=swa.SDPA_MASK_BOTTOM_RIGHT, s_q=512)
+    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_UNSUPPORTED
+
+
+def test_thd_needs_offsets():
+    p = base_params(layout=swa.SDPA_THD, total_q=300, total_kv=300)
+    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_INVALID_ARG
+    assert "offsets" in swa.last_error()

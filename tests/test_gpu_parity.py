@@ -1,0 +1,150 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on seeded
+inputs: element by element at sizes the oracle finishes in seconds (several
+tiles, ragged tails), and on sampled (batch, kv-head) units at the full sizes
+of the benchmark workloads. Covers every mask mode, window edge cases, GQA/MQA,
+BSHD padding, THD packing with gaps and empty sequences, sinks, f16/bf16,
+d = 64/128 and the deterministic relay (bitwise repeatable)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from swa_cases import Case, build, check_all, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sliding_window_attention_sdpa_gb300 as swa
+    swa.load()
+
+
+SMALL = [
+    Case("tiny_b1_h2_d64_s256_tl_w32", 1, 2, 2, 256, 256, 64, "tl", 32),
+    Case("tiny_b1_h2_d64_s256_tl_w32_det", 1, 2, 2, 256, 256, 64, "tl", 32, det=True),
+    Case("tl_w128_ragged_s700", 2, 4, 4, 700, 700, 64, "tl", 128, seed=1),
+    Case("tl_no_window_s300", 1, 2, 2, 300, 300, 64, "tl", -1, seed=2),
+    Case("tl_w0_s200", 1, 2, 2, 200, 200, 64, "tl", 0, seed=3),
+    Case("tl_w1_s200_f16", 1, 2, 2, 200, 200, 64, "tl", 1, dtype="f16", seed=4),
+    Case("br_w96_gqa8x2_d128_s1000", 2, 8, 2, 1000, 1000, 128, "br", 96, seed=5),
+    Case("br_w96_gqa8x2_d128_s1000_f16", 2, 8, 2, 1000, 1000, 128, "br", 96, dtype="f16", seed=6),
+    Case("br_nonsquare_q128_kv1100_w800", 2, 8, 2, 128, 1100, 64, "br", 800, seed=7),
+    Case("none_w200_s600", 1, 4, 4, 600, 600, 64, "none", 200, seed=8),
+    Case("none_w100_r30_s500_d128", 1, 2, 2, 500, 500, 128, "none", 100, 30, seed=9),
+    Case("tl_w50_r5_s400", 1, 2, 2, 400, 400, 64, "tl", 50, 5, seed=10),
+    Case("mqa_h4x1_tl_w64_s500", 2, 4, 1, 500, 500, 64, "tl", 64, seed=11),
+    Case("pad_br_w64_sink_gqa4x2", 2, 4, 2, 517, 517, 64, "br", 64, lens_q=[300, 517],
+         lens_kv=[450, 200], sink=True, seed=12),
+    Case("thd_gqa8x2_f16_tl_w128_sink_det", 0, 8, 2, 0, 0, 64, "tl", 128, dtype="f16",
+         layout="thd", thd_lens=[130, 1, 0, 700, 257], slot_align=128, sink=True, det=True,
+         seed=13),
+    Case("thd_d128_none_w300", 0, 4, 4, 0, 0, 128, "none", 300, layout="thd",
+         thd_lens=[390, 64, 1000], slot_align=8, seed=14),
+    Case("br_q_longer_than_kv_lens", 2, 2, 2, 400, 400, 64, "br", 40, lens_q=[400, 300],
+         lens_kv=[150, 400], seed=15),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: c.name)
+def test_small_parity(case):
+    bt = build(case)
+    out = run_gpu(bt)
+    check_all(bt, out)
+
+
+def test_deterministic_is_bitwise_repeatable_and_matches_nondet():
+    case = Case("det_tl_w128_s1000_gqa", 2, 8, 4, 1000, 1000, 64, "tl", 128, sink=True,
+                det=True, seed=20)
+    bt = build(case)
+    runs = [run_gpu(bt) for _ in range(3)]
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+    check_all(bt, runs[0])
+    nd = run_gpu(bt, deterministic=False)
+    for name, a, b in zip(("dq", "dk", "dv", "dsink"), runs[0], nd):
+        compare(name, a, b.double().cpu().numpy(), "bf16")
+
+
+def test_padding_values_never_leak():
+    """NaN in every padded row of Q, K, V, O, dO and LSE: results in the valid
+    region are unchanged and padded rows get zero gradients."""
+    case = Case("pad_nan", 2, 4, 4, 300, 300, 64, "br", 50, lens_q=[200, 300],
+                lens_kv=[260, 120], seed=21)
+    bt = build(case)
+    d = bt.dev
+    for bi, (lq, lk) in enumerate(zip(case.lens_q, case.lens_kv)):
+        for name in ("q", "o", "do"):
+            d[name][bi, lq:] = float("nan")
+        d["lse"][bi, :, lq:] = float("nan")
+        for name in ("k", "v"):
+            d[name][bi, lk:] = float("nan")
+    dq, dk, dv, _ = run_gpu(bt)
+    check_all(bt, (dq, dk, dv, None))
+    for bi, (lq, lk) in enumerate(zip(case.lens_q, case.lens_kv)):
+        assert not dq[bi, lq:].any() and not dk[bi, lk:].any() and not dv[bi, lk:].any()
+
+
+def test_strided_inputs():
+    """Q, K, V sliced out of one packed [b, s, 3, h, d] tensor (non-contiguous)."""
+    case = Case("strided", 1, 4, 4, 333, 333, 64, "tl", 70, seed=22)
+    bt = build(case)
+    d = bt.dev
+    packed = torch.stack([d["q"], d["k"], d["v"]], dim=2)  # [b, s, 3, h, d]
+    q, k, v = packed[:, :, 0], packed[:, :, 1], packed[:, :, 2]
+    assert not q.is_contiguous()
+    import sliding_window_attention_sdpa_gb300 as swa
+    out = swa.backward(q, k, v, d["o"], d["do"], d["lse"], check_status=True, **bt.kwargs)
+    check_all(bt, out)
+
+
+def test_empty_problem():
+    """A batch whose sequences are all empty runs and writes nothing."""
+    case = Case("thd_empty", 0, 2, 2, 0, 0, 64, "tl", 16, layout="thd", thd_lens=[0, 0],
+                slot_align=8, seed=23)
+    bt = build(case)
+    out = run_gpu(bt)
+    assert out[0].numel() == 0
+
+
+# ---- full-size workloads of the benchmark, sampled units
+
+FULL = [
+    (Case("gptoss_b2_h16_d64_w128_s8192", 2, 16, 16, 8192, 8192, 64, "tl", 128, seed=1001,
+          gen_device="cuda"), [(0, 3), (1, 15)]),
+    (Case("gptoss_b2_h16_d64_w128_s8192_det", 2, 16, 16, 8192, 8192, 64, "tl", 128, det=True,
+          seed=1001, gen_device="cuda"), [(1, 0)]),
+    (Case("gqa_b12_h48x6_d128_s16484_br_w96", 12, 48, 6, 16484, 16484, 128, "br", 96,
+          seed=1002, gen_device="cuda"), [(11, 5)]),
+    (Case("nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000", 12, 40, 8, 128, 8960, 64, "br", 8000,
+          seed=1003, gen_device="cuda"), [(0, 0), (7, 3)]),
+    (Case("winonly_b4_h16_d64_s4096_w512", 4, 16, 16, 4096, 4096, 64, "none", 512, seed=1004,
+          gen_device="cuda"), [(2, 9)]),
+]
+
+
+@pytest.mark.parametrize("case,units", FULL, ids=lambda x: x.name if isinstance(x, Case) else "")
+def test_full_size_sampled(case, units):
+    bt = build(case, units=units)
+    out = run_gpu(bt)
+    check_all(bt, out)
+    for t in out[:3]:
+        assert torch.isfinite(t).all()
+    del bt, out
+    torch.cuda.empty_cache()
+
+
+def test_thd_varlen_sinks_det_full_size():
+    from sliding_window_attention_sdpa_gb300 import inputs
+    lens = inputs.thd_lengths(16, 128, 8192, seed=1005).tolist()
+    case = Case("thd16_h64x8_d64_f16_tl_w128_sink_det", 0, 64, 8, 0, 0, 64, "tl", 128,
+                dtype="f16", layout="thd", thd_lens=lens, slot_align=128, sink=True, det=True,
+                seed=1005, gen_device="cuda")
+    units = [(bi, g) for bi in range(16) for g in (2,)]
+    bt = build(case, units=units)
+    out = run_gpu(bt)
+    check_all(bt, out)
