@@ -123,7 +123,8 @@ class Problem:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms while the GPU
+    runs the warm-up, the timed steps and the end-to-end leg."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -140,7 +141,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -361,10 +362,10 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         total, main_ms = time_device(prob, args.steps, args.warmup)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps // 2), 2)
     step_ms = sum(total) / len(total)
     main_avg = sum(main_ms) / len(main_ms)
-    e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps // 2), 2)
     status = swa.sdpa_bwd_check_status(prob.ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
     if dist is not None:

@@ -150,6 +150,11 @@ def _ptr(t) -> Optional[int]:
 def _strides(t, layout: int):
     if t is None:
         return (0, 0, 0)
+    if t.numel() == 0:  # no element is ever addressed: report packed strides
+        s = [1] * t.dim()
+        for i in range(t.dim() - 2, -1, -1):
+            s[i] = s[i + 1] * max(t.shape[i + 1], 1)
+        return (0, s[0], s[1]) if layout == SDPA_THD else (s[0], s[1], s[2])
     s = t.stride()
     if t.stride(-1) != 1:
         raise ValueError("the feature dimension must be contiguous (stride 1)")
