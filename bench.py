@@ -325,6 +325,16 @@ def aggregate(per_rank_ms, per_rank_flops):
     return sum(per_rank_flops) / (t * 1e-3) / 1e12, t
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise max of a list of floats over all ranks (identity without
+    a process group)."""
+    if dist is None:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,12 +378,7 @@ def main():
     main_avg = sum(main_ms) / len(main_ms)
     status = swa.sdpa_bwd_check_status(prob.ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
-    if dist is not None:
-        t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_max, e2e_max = t.tolist()
-    else:
-        step_max, e2e_max = step_ms, e2e_ms
+    step_max, e2e_max = max_over_ranks([step_ms, e2e_ms], dist, dev)
     value, _ = aggregate([step_max], [prob.flops * world])
     e2e_val, _ = aggregate([e2e_max], [prob.flops * world])
 

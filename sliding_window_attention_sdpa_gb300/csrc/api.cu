@@ -5,8 +5,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/sdpa_bwd.h"
@@ -206,6 +208,58 @@ sdpa_status_t cuda_status(cudaError_t e, const char* what)
     return fail(SDPA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// TMA descriptor of one head-strided 16-bit tensor: 64 x 1 x 128 (x 1) boxes,
+// 128-byte swizzle, zero fill outside the tensor. Sizes of 1 get a harmless
+// non-zero stride.
+sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int dtype, bool thd,
+                       int64_t d, int64_t h, int64_t rows, int64_t b, const int64_t* st)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const CUtensorMapDataType dt =
+        dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(d) * 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                          static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(b)};
+    cuuint64_t hs = h > 1 ? static_cast<cuuint64_t>(st[2]) * 2 : row_bytes;
+    cuuint64_t ss = rows > 1 ? static_cast<cuuint64_t>(st[1]) * 2 : hs * h;
+    cuuint64_t bs = b > 1 ? static_cast<cuuint64_t>(st[0]) * 2 : ss * (rows > 0 ? rows : 1);
+    cuuint64_t strides[3] = {hs, ss, bs};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint32_t rank = thd ? 3 : 4;
+    CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SDPA_ERR_UNSUPPORTED,
+                    "%s: TMA descriptor rejected (error %d) for strides (%lld, %lld, %lld)", name,
+                    (int)r, (long long)st[0], (long long)st[1], (long long)st[2]);
+    return SDPA_OK;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
@@ -287,6 +341,23 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     a.scale_log2 = p->scale * 1.4426950408889634f;
     a.deterministic = p->deterministic;
     a.timeout_ns = 2000000000LL;
+    if (p->b * p->h_q * a.n_kv_tiles == 0) return SDPA_OK;
+    const bool thd = p->layout == SDPA_THD;
+    const int64_t rq = thd ? p->total_q : p->s_q, rk = thd ? p->total_kv : p->s_kv;
+    if (rk == 0) return SDPA_OK;  // no keys: dK, dV are empty and dQ stays zero
+    // With no q rows the main kernel only writes dK = dV = 0; Q and dO then get
+    // placeholder descriptors over K that are never used.
+    const int64_t rq_map = rq > 0 ? rq : 1, rk_map = rk;
+    const void* qptr = rq > 0 ? p->q : p->k;
+    const void* doptr = rq > 0 ? p->dout : p->k;
+    const int64_t* qst = rq > 0 ? p->q_stride : p->k_stride;
+    const int64_t* dost = rq > 0 ? p->do_stride : p->k_stride;
+    const int64_t hq_map = rq > 0 ? p->h_q : p->h_kv;
+    if ((st = make_map(&a.tm_q, "q", qptr, p->dtype, thd, p->d, hq_map, rq_map, p->b, qst)) != SDPA_OK ||
+        (st = make_map(&a.tm_do, "dout", doptr, p->dtype, thd, p->d, hq_map, rq_map, p->b, dost)) != SDPA_OK ||
+        (st = make_map(&a.tm_k, "k", p->k, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->k_stride)) != SDPA_OK ||
+        (st = make_map(&a.tm_v, "v", p->v, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->v_stride)) != SDPA_OK)
+        return st;
     return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
 }
 

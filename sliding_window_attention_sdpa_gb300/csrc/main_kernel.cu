@@ -1,30 +1,37 @@
 // main_kernel.cu -- fused sliding-window SDPA backward on sm_103a tensor cores.
 //
-// One CTA per work item (kv-tile t, q-head h, sequence b). The kv-tile's K and
-// V rows stay in shared memory; the CTA sweeps the q-tiles in the window-clamped
-// range [q_lo, q_hi) (cuDNN-frontend PR #866, "Change": no query with
-// anchor > kv_base + tile_kv - 1 + W reaches the tile), and for each q-tile
-// issues the five contractions as tcgen05.mma with fp32 accumulators in tensor
-// memory (TMEM):
+// Work item = (kv-tile t, q-head h, sequence b). A persistent CTA (one per SM)
+// walks its items; for each it keeps the kv-tile's K and V in shared memory and
+// sweeps the q-tiles in the window-clamped range [q_lo, q_hi) (cuDNN-frontend
+// PR #866, "Change": no query with anchor > kv_base + tile_kv - 1 + W reaches
+// the tile), issuing the five contractions as tcgen05.mma with fp32
+// accumulators in tensor memory (TMEM):
 //
-//   S^T  = K Q^T          [kv x q]   TMEM cols   0..127
-//   dP^T = V dO^T         [kv x q]   TMEM cols 128..255
-//   dV  += P^T dO         [kv x d]   TMEM cols 256..256+d
-//   dK  += dS^T Q         [kv x d]   TMEM cols 256+d..256+2d
-//   dQ   = dS K           [q x d]    TMEM cols   0..d (reuses S^T once read)
+//   S^T  = K Q^T     [kv x q]  cols   0..127
+//   dP^T = V dO^T    [kv x q]  cols 128..255
+//   dV  += P^T dO    [kv x d]  cols 256..
+//   dK  += dS^T Q    [kv x d]  cols 256+d..
+//   dQ   = dS K      [q x d]   cols 384.. (d = 64) or aliasing S^T (d = 128)
 //
-// Between them the 128 threads (one per TMEM lane = kv row) recompute
-// P = exp(S*scale - LSE) and dS = P (dP - D) in registers, apply the mask
-// (top-left / bottom-right causal with left window, window-only, right band,
-// padding) and write P^T and dS^T to shared memory as 16-bit operands. dQ rows
-// are added to the fp32 accumulator with vector atomics, or in deterministic
-// mode through the ordered relay whose turn is t - kv_first(q-tile).
+// Warp roles (384 threads):
+//   warp 0      TMA producer: K, V per item; Q, dO per q-tile into a ring of
+//               kStages stages (128-byte swizzle, zero fill past the tensor)
+//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warps 2-3   LSE / D loader: the q-tile's 128 LSE (log2 domain) and D values
+//   warps 4-7   softmax: one thread per kv row (TMEM lane) recomputes
+//               P = exp2(S*scale*log2e - LSE*log2e) and dS = P (dP - D) with
+//               the mask, writes P^T / dS^T as swizzled 16-bit tiles; at the end
+//               of an item stores dK, dV (or fp32 GQA partials)
+//   warps 8-11  dQ: one thread per q row reads dQ from TMEM and adds it to the
+//               fp32 accumulator (vector atomics, or the ordered relay)
+// Hand-offs are mbarriers; every wait is bounded (status word on timeout).
 //
-// Shared-memory operands use the 128-byte swizzled layout: rows of 64 16-bit
-// elements (128 B), 8-row atoms of 1024 B, 16-byte chunk c of row r stored at
-// chunk position c ^ (r % 8); 64-column blocks of a 128-row tile are 16 KB apart.
-// The same buffer serves as a K-major operand (contraction along the row) or
-// an MN-major one (contraction across rows) through different descriptors.
+// Shared-memory operand layout: rows of 64 16-bit elements (128 B), 8-row
+// atoms of 1024 B, 16-byte chunk c of row r at chunk position c ^ (r % 8)
+// (the TMA 128-byte swizzle); 64-column blocks of a 128-row tile 16 KB apart.
+// One buffer serves as a K-major operand or, through another descriptor, as an
+// MN-major one.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,50 +43,45 @@ namespace swa {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
 constexpr uint32_t kBlock16K = 128 * 128;  // one 64-column block of a 128-row tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+// warp roles
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLse0 = 2, kWarpSoft0 = 4, kWarpDq0 = 8;
+constexpr int kLseThreads = 64;
+constexpr int kBarDq = 1, kBarSoft = 2;  // named barriers of the two 128-thread groups
 
 template <int HD>
-struct Smem {
+struct Cfg {
+    static constexpr int kStages = HD == 64 ? 2 : 1;    // Q/dO/LSE/D ring
+    static constexpr int kKvStages = HD == 64 ? 2 : 1;  // K/V ring (per work item)
     static constexpr uint32_t kTile = 128 * HD * 2;
-    static constexpr uint32_t kK = 0;
-    static constexpr uint32_t kV = kK + kTile;
-    static constexpr uint32_t kQ = kV + kTile;
-    static constexpr uint32_t kDO = kQ + kTile;
-    static constexpr uint32_t kP = kDO + kTile;     // P^T  [128 kv x 128 q]
-    static constexpr uint32_t kDS = kP + 32768;     // dS^T [128 kv x 128 q]
-    static constexpr uint32_t kLse = kDS + 32768;   // 128 fp32 (log2 domain)
-    static constexpr uint32_t kDelta = kLse + 512;  // 128 fp32
-    static constexpr uint32_t kBar = kDelta + 512;  // mbarrier (8 B)
-    static constexpr uint32_t kMisc = kBar + 16;    // tmem slot, item, flags
+    // shared memory offsets (from a 1024-aligned base)
+    static constexpr uint32_t kK = 0;                           // kKvStages tiles
+    static constexpr uint32_t kV = kK + kKvStages * kTile;      // kKvStages tiles
+    static constexpr uint32_t kQ = kV + kKvStages * kTile;      // kStages tiles
+    static constexpr uint32_t kDO = kQ + kStages * kTile;       // kStages tiles
+    static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q]
+    static constexpr uint32_t kDS = kP + 32768;                 // dS^T [128 kv x 128 q]
+    static constexpr uint32_t kLse = kDS + 32768;               // kStages x 128 fp32
+    static constexpr uint32_t kDelta = kLse + kStages * 512;    // kStages x 128 fp32
+    static constexpr uint32_t kBars = kDelta + kStages * 512;   // mbarriers
+    static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags
     static constexpr uint32_t kBytes = kMisc + 64;
-    static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-B alignment
+    static constexpr uint32_t kAlloc = kBytes + 1024;
+    // TMEM columns
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
+    static constexpr uint32_t kColDQ = HD == 64 ? 384 : 0;
+    static constexpr bool kDqAliasesS = HD != 64;
 };
 
-__device__ __forceinline__ uint32_t swz(int r, int chunk)
-{
-    // byte offset of 16-byte chunk `chunk` (0..HD/8-1) of row r in a 128-row tile
-    return static_cast<uint32_t>((chunk >> 3) * kBlock16K + (r >> 3) * 1024 + (r & 7) * 128 +
-                                 (((chunk & 7) ^ (r & 7)) << 4));
-}
-
-// Copies rows [0, 128) of a row-strided [., HD] 16-bit matrix into a swizzled
-// tile; rows at or past `nvalid` are zero.
-template <int HD>
-__device__ __forceinline__ void load_tile(uint8_t* dst, const uint16_t* src, int64_t row_stride,
-                                          int64_t nvalid, int tid)
-{
-    constexpr int CPR = HD / 8;
-#pragma unroll 4
-    for (int idx = tid; idx < 128 * CPR; idx += kThreads) {
-        const int r = idx / CPR, c = idx % CPR;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nvalid) v = ld_nc_v4(src + r * row_stride + c * 8);
-        *reinterpret_cast<uint4*>(dst + swz(r, c)) = v;
-    }
-}
+// mbarrier indices
+enum Bar : int {
+    kSFull = 0, kPFull, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
+    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kNumBars
+};
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
@@ -90,6 +92,65 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t swz(int r, int chunk)
+{
+    return static_cast<uint32_t>((chunk >> 3) * kBlock16K + (r >> 3) * 1024 + (r & 7) * 128 +
+                                 (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Loads rows [row, row + 128) of one head of a [., HD] tensor into a swizzled tile
+// (HD/64 boxes of 64 columns). BSHD maps are 4-D (d, h, s, b); THD maps 3-D (d, h, t).
+template <int HD>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                         bool thd, int head, int row, int batch)
+{
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb) {
+        if (thd) tma_load_3d(dst + cb * kBlock16K, map, bar, cb * 64, head, row);
+        else tma_load_4d(dst + cb * kBlock16K, map, bar, cb * 64, head, row, batch);
+    }
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier over `count` threads (named barrier `id`) returning the AND of `v`.
+__device__ __forceinline__ bool bar_and(int id, int count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // q-tile range [lo, hi) of kv rows [kv_base, kv_end) of one sequence: lo is
@@ -116,303 +177,432 @@ __device__ __forceinline__ void q_range(const Geometry& g, const SeqInfo& s, int
     if (hi < lo) hi = lo;
 }
 
+struct Item {
+    int64_t t, h, bi, gk;
+    SeqInfo s;
+    int64_t kv_base, q_lo, q_hi;
+    bool has_work;   // at least one q-tile to sweep
+    bool in_slot;    // the kv-tile has rows inside the sequence's slot
+};
+
+__device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
+{
+    const Geometry& g = a.g;
+    Item it;
+    it.t = item % a.n_kv_tiles;
+    it.h = (item / a.n_kv_tiles) % g.h_q;
+    it.bi = item / (a.n_kv_tiles * g.h_q);
+    it.gk = it.h / (g.h_q / g.h_kv);
+    it.s = seq_info(g, it.bi);
+    it.kv_base = it.t * kTileKV;
+    const int64_t kv_end = imin(it.kv_base + kTileKV, it.s.len_kv);
+    q_range(g, it.s, it.kv_base, kv_end, it.q_lo, it.q_hi);
+    it.in_slot = it.kv_base < it.s.slot_kv;
+    it.has_work = it.q_hi > it.q_lo && it.in_slot;
+    return it;
+}
+
+// Zeroes rows [nvalid, 128) of a swizzled tile (whole 128-byte rows, so the
+// swizzle does not matter); run by one warp, then made visible to the tensor
+// core. Used where rows past a sequence end hold data of another sequence
+// or padding (TMA fills only past the tensor's extent).
+template <int HD>
+__device__ __forceinline__ void zero_tail(uint8_t* tile, int64_t nvalid, int lane)
+{
+    const int first = nvalid < 0 ? 0 : static_cast<int>(nvalid);
+    if (first >= 128) return;
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb) {
+        uint4* p = reinterpret_cast<uint4*>(tile + cb * kBlock16K + first * 128);
+        const int n16 = (128 - first) * 8;
+        for (int k = lane; k < n16; k += 32) p[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
 }  // namespace
 
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a)
 {
-    using L = Smem<HD>;
+    using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* sLse = reinterpret_cast<float*>(sm + L::kLse);
-    float* sDelta = reinterpret_cast<float*>(sm + L::kDelta);
-    const uint32_t bar = sbase + L::kBar;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + L::kMisc);  // [0] tmem, [1] item, [2] flag
+    const uint32_t bars = sbase + C::kBars;
+    auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kMisc);  // [0] tmem base, [1] abort flag
 
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint64_t tmo = static_cast<uint64_t>(a.timeout_ns);
+    const int64_t n_items = g.b * g.h_q * a.n_kv_tiles;
+    const bool thd = g.layout == 1;
 
     if (tid == 0) {
-        misc[1] = a.deterministic ? static_cast<uint32_t>(atomicAdd(&a.status[1], 1)) : blockIdx.x;
-        misc[2] = 0;
-        mbar_init(bar, 1);
+        misc[1] = 0;
+        for (int s = 0; s < C::kKvStages; ++s) {
+            mbar_init(bar(kKvFull0 + s), 1);
+            mbar_init(bar(kKvEmpty0 + s), 1);
+        }
+        mbar_init(bar(kSFull), 1);
+        mbar_init(bar(kPFull), 128);
+        mbar_init(bar(kDqFull), 1);
+        mbar_init(bar(kDqEmpty), 128);
+        mbar_init(bar(kAccFull), 1);
+        mbar_init(bar(kAccEmpty), 128);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(kQFull0 + s), 1 + kLseThreads);
+            mbar_init(bar(kQEmpty0 + s), 1);
+        }
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tmem_alloc(sbase + L::kMisc, kTmemCols);
+    if (warp == kWarpMma) {
+        tmem_alloc(sbase + C::kMisc, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int64_t item = misc[1];
+    volatile uint32_t* abort_flag = misc + 1;
 
-    const int64_t t = item % a.n_kv_tiles;
-    const int64_t h = (item / a.n_kv_tiles) % g.h_q;
-    const int64_t bi = item / (a.n_kv_tiles * g.h_q);
-    const int64_t gk = h / (g.h_q / g.h_kv);
-    const SeqInfo s = seq_info(g, bi);
-    if (s.bad && t == 0 && h == 0 && tid == 0) set_status(a.status, kStatusBadLengths);
-
-    const int64_t kv_base = t * kTileKV;
-    const int64_t kv_end = imin(kv_base + kTileKV, s.len_kv);
-    int64_t q_lo, q_hi;
-    q_range(g, s, kv_base, kv_end, q_lo, q_hi);
-    const bool has_work = q_hi > q_lo && kv_base < s.slot_kv;
-
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tm_s = tmem + kColS, tm_dp = tmem + kColDP;
-    const uint32_t tm_dv = tmem + kColDV, tm_dk = tmem + kColDV + HD, tm_dq = tmem + kColS;
-    constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
-    constexpr uint32_t kIdPV = idesc_f16(BF16, 128, HD, false, true);
-    constexpr uint32_t kIdDQ = idesc_f16(BF16, 128, HD, true, true);
-
-    const uint16_t* qp = static_cast<const uint16_t*>(a.q);
-    const uint16_t* kp = static_cast<const uint16_t*>(a.k);
-    const uint16_t* vp = static_cast<const uint16_t*>(a.v);
-    const uint16_t* dop = static_cast<const uint16_t*>(a.dout);
-    // element offsets of row 0 of the sequence's slot for the head in use
-    auto seq_base = [&](const int64_t* st, int64_t row0_packed, int64_t head) -> int64_t {
-        return (g.layout == 1 ? row0_packed * st[1] : bi * st[0]) + head * st[2];
+    // A wait that gives up marks the CTA aborted; later waits of every role
+    // return at once so that the kernel drains and frees TMEM.
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar(b), parity, tmo)) return true;
+        *abort_flag = 1;
+        set_status(a.status, kStatusTimeout);
+        return false;
     };
-    const int64_t kbase = seq_base(a.k_stride, s.kv_row0, gk);
-    const int64_t vbase = seq_base(a.v_stride, s.kv_row0, gk);
-    const int64_t qbase = seq_base(a.q_stride, s.q_row0, h);
-    const int64_t dobase = seq_base(a.do_stride, s.q_row0, h);
+    auto wait_warp = [&](int b, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(b, parity));
+    };
+    auto wait_group = [&](int id, int b, uint32_t parity) -> bool {
+        return bar_and(id, 128, wait(b, parity));
+    };
 
-    // this thread's kv row and the q rows it attends: [i_lo, i_hi]
-    const int64_t kj = kv_base + tid;
-    int64_t i_lo = 0, i_hi = s.len_q - 1;
-    if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - s.diag);
-    if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - s.diag);
-    if (kj >= s.len_kv) i_hi = -1;
-
-    uint32_t phase = 0;
-    bool ok = true;
-
-    if (has_work) {
-        load_tile<HD>(sm + L::kK, kp + kbase + kv_base * a.k_stride[1], a.k_stride[1],
-                      s.len_kv - kv_base, tid);
-        load_tile<HD>(sm + L::kV, vp + vbase + kv_base * a.v_stride[1], a.v_stride[1],
-                      s.len_kv - kv_base, tid);
-    }
-
-#pragma unroll 1
-    for (int64_t j = q_lo; j < q_hi && ok; ++j) {
-        const int64_t q0 = j * kTileQ;
-        // ---- stage Q, dO, LSE, D of q-tile j
-        load_tile<HD>(sm + L::kQ, qp + qbase + q0 * a.q_stride[1], a.q_stride[1], s.len_q - q0, tid);
-        load_tile<HD>(sm + L::kDO, dop + dobase + q0 * a.do_stride[1], a.do_stride[1],
-                      s.len_q - q0, tid);
-        {
-            const int64_t qi = q0 + tid;
-            float lse = INFINITY, dlt = 0.f;
-            if (qi < s.len_q) {
-                const int64_t st = stat_offset(g, s.q_row0 + qi, h);
-                lse = a.lse[st];
-                dlt = a.delta[st];
-                if (lse == -INFINITY) lse = INFINITY;  // row attends nothing: P = 0
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_it = 0;
+            for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+                const Item it = decode(a, item);
+                if (!it.has_work) continue;
+                const int ks = kv_it % C::kKvStages;
+                if (!wait(kKvEmpty0 + ks, ((kv_it / C::kKvStages) & 1) ^ 1)) break;
+                ++kv_it;
+                const int kvrow = static_cast<int>((thd ? it.s.kv_row0 : 0) + it.kv_base);
+                mbar_arrive_expect_tx(bar(kKvFull0 + ks), 2 * C::kTile);
+                tma_tile<HD>(sbase + C::kK + ks * C::kTile, &a.tm_k, bar(kKvFull0 + ks), thd,
+                             (int)it.gk, kvrow, (int)it.bi);
+                tma_tile<HD>(sbase + C::kV + ks * C::kTile, &a.tm_v, bar(kKvFull0 + ks), thd,
+                             (int)it.gk, kvrow, (int)it.bi);
+                bool ok = true;
+                for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                    const int st = q_it % C::kStages;
+                    if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
+                    const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
+                    mbar_arrive_expect_tx(bar(kQFull0 + st), 2 * C::kTile);
+                    tma_tile<HD>(sbase + C::kQ + st * C::kTile, &a.tm_q, bar(kQFull0 + st), thd,
+                                 (int)it.h, qrow, (int)it.bi);
+                    tma_tile<HD>(sbase + C::kDO + st * C::kTile, &a.tm_do, bar(kQFull0 + st), thd,
+                                 (int)it.h, qrow, (int)it.bi);
+                }
+                if (!ok) break;
             }
-            sLse[tid] = lse * 1.4426950408889634f;
-            sDelta[tid] = dlt;
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- S^T = K Q^T, dP^T = V dO^T
-        if (tid == 0) {
-            tc_fence_after();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
+        constexpr uint32_t kIdPV = idesc_f16(BF16, 128, HD, false, true);
+        constexpr uint32_t kIdDQ = idesc_f16(BF16, 128, HD, true, true);
+        const uint32_t tm_s = tmem + C::kColS, tm_dp = tmem + C::kColDP;
+        const uint32_t tm_dv = tmem + C::kColDV, tm_dk = tmem + C::kColDK, tm_dq = tmem + C::kColDQ;
+        uint32_t kv_it = 0, q_it = 0, p_it = 0, dq_it = 0, acc_it = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode(a, item);
+            if (!it.has_work) continue;
+            const int ks = kv_it % C::kKvStages;
+            if (!(ok = wait_warp(kKvFull0 + ks, (kv_it / C::kKvStages) & 1))) break;
+            ++kv_it;
+            const uint32_t sK = sbase + C::kK + ks * C::kTile, sV = sbase + C::kV + ks * C::kTile;
+            if (it.kv_base + kTileKV > it.s.len_kv)
+                zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
+            for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                const int st = q_it % C::kStages;
+                if (!(ok = wait_warp(kQFull0 + st, (q_it / C::kStages) & 1))) break;
+                const int64_t q0 = j * kTileQ;
+                if (q0 + kTileQ > it.s.len_q) {
+                    zero_tail<HD>(sm + C::kQ + st * C::kTile, it.s.len_q - q0, lane);
+                    zero_tail<HD>(sm + C::kDO + st * C::kTile, it.s.len_q - q0, lane);
+                }
+                // S^T and dP^T overwrite TMEM that the previous dQ may alias
+                if (C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
+                const uint32_t sQ = sbase + C::kQ + st * C::kTile, sDO = sbase + C::kDO + st * C::kTile;
+                if (lane == 0) {
+                    tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k) {
-                const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                umma_f16_ss(tm_s, sdesc_sw128(sbase + L::kK + koff, 16, 1024),
-                            sdesc_sw128(sbase + L::kQ + koff, 16, 1024), kIdQK, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < HD / 16; ++k) {
-                const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                umma_f16_ss(tm_dp, sdesc_sw128(sbase + L::kV + koff, 16, 1024),
-                            sdesc_sw128(sbase + L::kDO + koff, 16, 1024), kIdQK, k > 0);
-            }
-            umma_commit(bar);
-        }
-        ok = __syncthreads_and(mbar_wait(bar, phase, a.timeout_ns));
-        phase ^= 1;
-        if (!ok) break;
-        tc_fence_after();
-
-        // ---- P^T, dS^T rows of this thread's kv row
-        {
-            const int64_t c_lo = imax(i_lo - q0, 0);
-            const int64_t c_hi = imin(i_hi - q0, 127);
-            uint8_t* prow = sm + L::kP;
-            uint8_t* dsrow = sm + L::kDS;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(tm_s + lane_off + ch * 32, sv);
-                tmem_ld32(tm_dp + lane_off + ch * 32, dpv);
-                tmem_ld_wait();
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p2[2], d2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = ch * 32 + e + u;
-                        const bool att = c >= c_lo && c <= c_hi;
-                        const float sc = __uint_as_float(sv[e + u]);
-                        const float dp = __uint_as_float(dpv[e + u]);
-                        const float p = att ? ex2_approx(fmaf(sc, a.scale_log2, -sLse[c])) : 0.f;
-                        p2[u] = p;
-                        d2[u] = att ? p * (dp - sDelta[c]) : 0.f;
+                    for (int k = 0; k < HD / 16; ++k) {
+                        const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_s, sdesc_sw128(sK + koff, 16, 1024),
+                                    sdesc_sw128(sQ + koff, 16, 1024), kIdQK, k > 0);
                     }
-                    pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
-                    dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);
-                }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t off = swz(tid, ch * 4 + m);
-                    *reinterpret_cast<uint4*>(prow + off) =
-                        make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
-                    *reinterpret_cast<uint4*>(dsrow + off) =
-                        make_uint4(dk[4 * m], dk[4 * m + 1], dk[4 * m + 2], dk[4 * m + 3]);
+                    for (int k = 0; k < HD / 16; ++k) {
+                        const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_dp, sdesc_sw128(sV + koff, 16, 1024),
+                                    sdesc_sw128(sDO + koff, 16, 1024), kIdQK, k > 0);
+                    }
+                    umma_commit(bar(kSFull));
                 }
+                __syncwarp();
+                // P^T, dS^T ready in shared memory (softmax done with S^T, dP^T)
+                if (!(ok = wait_warp(kPFull, p_it & 1))) break;
+                ++p_it;
+                if (!C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
+                if (j == it.q_lo && !(ok = wait_warp(kAccEmpty, (acc_it & 1) ^ 1))) break;
+                ++dq_it;
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t acc = j > it.q_lo ? 1u : 0u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024),
+                                    sdesc_sw128(sDO + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_dk, sdesc_sw128(sbase + C::kDS + aoff, 16, 1024),
+                                    sdesc_sw128(sQ + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        umma_f16_ss(tm_dq, sdesc_sw128(sbase + C::kDS + k * 2048, kBlock16K, 1024),
+                                    sdesc_sw128(sK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
+                    umma_commit(bar(kDqFull));
+                    umma_commit(bar(kQEmpty0 + st));
+                    if (j + 1 == it.q_hi) {
+                        umma_commit(bar(kAccFull));
+                        umma_commit(bar(kKvEmpty0 + ks));
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            ++acc_it;
+        }
+    } else if (warp < kWarpSoft0) {
+        // ------------------------------------------------------------ LSE / D loader
+        const int lt = tid - kWarpLse0 * 32;  // 0..63, two rows each
+        uint32_t q_it = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode(a, item);
+            if (!it.has_work) continue;
+            for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                const int st = q_it % C::kStages;
+                if (!(ok = wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1))) break;
+                float* sl = reinterpret_cast<float*>(sm + C::kLse + st * 512);
+                float* sd = reinterpret_cast<float*>(sm + C::kDelta + st * 512);
+#pragma unroll
+                for (int r = lt; r < 128; r += kLseThreads) {
+                    const int64_t qi = j * kTileQ + r;
+                    float lse = INFINITY, dlt = 0.f;
+                    if (qi < it.s.len_q) {
+                        const int64_t so = stat_offset(g, it.s.q_row0 + qi, it.h);
+                        lse = a.lse[so];
+                        dlt = a.delta[so];
+                        if (lse == -INFINITY) lse = INFINITY;  // row attends nothing: P = 0
+                    }
+                    sl[r] = lse * kLog2e;
+                    sd[r] = dlt;
+                }
+                mbar_arrive(bar(kQFull0 + st));
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- dV += P^T dO, dK += dS^T Q, dQ = dS K
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t acc = j > q_lo ? 1u : 0u;
+    } else if (warp < kWarpDq0) {
+        // ------------------------------------------------------------ softmax + dK/dV epilogue
+        const int r = tid - kWarpSoft0 * 32;  // kv row within the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint32_t q_it = 0, s_it = 0, acc_it = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const Item it = decode(a, item);
+            const int64_t kj = it.kv_base + r;
+            if (r == 0 && it.s.bad && it.t == 0 && it.h == 0) set_status(a.status, kStatusBadLengths);
+            if (it.has_work && ok) {
+                int64_t i_lo = 0, i_hi = it.s.len_q - 1;
+                if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - it.s.diag);
+                if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - it.s.diag);
+                if (kj >= it.s.len_kv) i_hi = -1;
+                for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                    const int st = q_it % C::kStages;
+                    if (!(ok = wait_group(kBarSoft, kQFull0 + st, (q_it / C::kStages) & 1))) break;
+                    if (!(ok = wait_group(kBarSoft, kSFull, s_it & 1))) break;
+                    ++s_it;
+                    tc_fence_after();
+                    const float* sl = reinterpret_cast<const float*>(sm + C::kLse + st * 512);
+                    const float* sd = reinterpret_cast<const float*>(sm + C::kDelta + st * 512);
+                    const int64_t q0 = j * kTileQ;
+                    const int64_t c_lo = imax(i_lo - q0, 0);
+                    const int64_t c_hi = imin(i_hi - q0, 127);
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t sv[32], dpv[32];
+                        tmem_ld32(tmem + C::kColS + lane_off + ch * 32, sv);
+                        tmem_ld32(tmem + C::kColDP + lane_off + ch * 32, dpv);
+                        tmem_ld_wait();
+                        uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                umma_f16_ss(tm_dv, sdesc_sw128(sbase + L::kP + aoff, 16, 1024),
-                            sdesc_sw128(sbase + L::kDO + k * 2048, kBlock16K, 1024), kIdPV,
-                            acc | (k > 0));
-            }
+                        for (int e = 0; e < 32; e += 2) {
+                            float p2[2], d2[2];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                umma_f16_ss(tm_dk, sdesc_sw128(sbase + L::kDS + aoff, 16, 1024),
-                            sdesc_sw128(sbase + L::kQ + k * 2048, kBlock16K, 1024), kIdPV,
-                            acc | (k > 0));
-            }
+                            for (int u = 0; u < 2; ++u) {
+                                const int c = ch * 32 + e + u;
+                                const bool att = c >= c_lo && c <= c_hi;
+                                const float p = att ? ex2_approx(fmaf(__uint_as_float(sv[e + u]),
+                                                                     a.scale_log2, -sl[c]))
+                                                    : 0.f;
+                                p2[u] = p;
+                                d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - sd[c]) : 0.f;
+                            }
+                            pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
+                            dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);
+                        }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                umma_f16_ss(tm_dq, sdesc_sw128(sbase + L::kDS + k * 2048, kBlock16K, 1024),
-                            sdesc_sw128(sbase + L::kK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
-            }
-            umma_commit(bar);
-        }
-        ok = __syncthreads_and(mbar_wait(bar, phase, a.timeout_ns));
-        phase ^= 1;
-        if (!ok) break;
-        tc_fence_after();
-
-        // ---- dQ rows (this thread: q row q0 + tid) into the fp32 accumulator
-        {
-            const int64_t qi = q0 + tid;
-            const bool row_ok = qi < s.len_q;
-            float* dst = a.dq_acc + ((s.q_row0 + qi) * g.h_q + h) * HD;
-            bool turn_ok = true;
-            int* sem = nullptr;
-            int turn = 0;
-            if (a.deterministic) {
-                const int64_t first = g.window_left >= 0
-                                          ? imax(floor_div(q0 + s.diag - g.window_left, kTileKV), 0)
-                                          : 0;
-                turn = static_cast<int>(t - first);
-                sem = a.sems + (bi * g.h_q + h) * a.n_q_tiles + j;
-                if (tid == 0) {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (ld_acquire_gpu(sem) != turn) {
-                        if (globaltimer_ns() - t0 > static_cast<uint64_t>(a.timeout_ns)) {
-                            set_status(a.status, kStatusTimeout);
-                            misc[2] = 1;
-                            break;
+                        for (int m = 0; m < 4; ++m) {
+                            const uint32_t off = swz(r, ch * 4 + m);
+                            *reinterpret_cast<uint4*>(sm + C::kP + off) =
+                                make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
+                            *reinterpret_cast<uint4*>(sm + C::kDS + off) =
+                                make_uint4(dk[4 * m], dk[4 * m + 1], dk[4 * m + 2], dk[4 * m + 3]);
                         }
                     }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(bar(kPFull));
                 }
-                __syncthreads();
-                turn_ok = misc[2] == 0;
+                if (ok) ok = wait_group(kBarSoft, kAccFull, acc_it & 1);
+                ++acc_it;
+                if (ok) tc_fence_after();
             }
+            // epilogue: dV, dK (scaled) of this thread's kv row
+            if (!it.in_slot) continue;
+            const bool live = it.has_work && ok && kj < it.s.len_kv;
+            const bool row_in_slot = kj < it.s.slot_kv;
+            const int64_t prow = it.s.kv_row0 + kj;
 #pragma unroll 1
-            for (int ch = 0; ch < HD / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(tm_dq + lane_off + ch * 32, v);
-                tmem_ld_wait();
-                if (row_ok && turn_ok) {
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = tmem + (which == 0 ? C::kColDV : C::kColDK);
+                const float mul = which == 0 ? 1.f : a.scale;
+#pragma unroll 1
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    uint32_t v[32];
+                    if (it.has_work && ok) {
+                        tmem_ld32(col + lane_off + ch * 32, v);
+                        tmem_ld_wait();
+                    }
+                    float f[32];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_v4(dst + ch * 32 + e, __uint_as_float(v[e]) * a.scale,
-                                   __uint_as_float(v[e + 1]) * a.scale,
-                                   __uint_as_float(v[e + 2]) * a.scale,
-                                   __uint_as_float(v[e + 3]) * a.scale);
+                    for (int e = 0; e < 32; ++e) f[e] = live ? __uint_as_float(v[e]) * mul : 0.f;
+                    if (!row_in_slot) continue;
+                    if (a.dk_ws != nullptr) {
+                        float* dst = (which == 0 ? a.dv_ws : a.dk_ws) + (prow * g.h_q + it.h) * HD + ch * 32;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(dst + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                    } else {
+                        const int64_t* sst = which == 0 ? a.dv_stride : a.dk_stride;
+                        uint16_t* base = static_cast<uint16_t*>(which == 0 ? a.dv : a.dk);
+                        uint16_t* dst = base + (thd ? prow * sst[1] : it.bi * sst[0] + kj * sst[1]) +
+                                        it.gk * sst[2] + ch * 32;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            *reinterpret_cast<uint4*>(dst + e) =
+                                make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
+                                           pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
+                    }
                 }
             }
-            if (a.deterministic) {
-                __threadfence();
-                __syncthreads();
-                if (tid == 0) st_release_gpu(sem, turn + 1);
+            if (it.has_work && ok) {
+                tc_fence_before();
+                mbar_arrive(bar(kAccEmpty));
             }
         }
-        tc_fence_before();
-        __syncthreads();
-    }
-
-    // ---- epilogue: dV, dK (scaled) rows of this thread's kv row
-    if (kv_base < s.slot_kv) {
-        const bool row_in_slot = kj < s.slot_kv;
-        const bool live = has_work && ok && kj < s.len_kv;
-        const int64_t prow = s.kv_row0 + kj;  // packed kv row
+    } else {
+        // ------------------------------------------------------------ dQ
+        const int r = tid - kWarpDq0 * 32;  // q row within the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint32_t dq_it = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode(a, item);
+            if (!it.has_work) continue;
+            for (int64_t j = it.q_lo; j < it.q_hi; ++j) {
+                if (!(ok = wait_group(kBarDq, kDqFull, dq_it & 1))) break;
+                ++dq_it;
+                tc_fence_after();
+                const int64_t q0 = j * kTileQ;
+                const int64_t qi = q0 + r;
+                const bool row_ok = qi < it.s.len_q;
+                float* dst = a.dq_acc + ((it.s.q_row0 + qi) * g.h_q + it.h) * HD;
+                int32_t* sem = nullptr;
+                int turn = 0;
+                bool turn_ok = true;
+                if (a.deterministic) {
+                    const int64_t first = g.window_left >= 0
+                        ? imax(floor_div(q0 + it.s.diag - g.window_left, kTileKV), 0) : 0;
+                    turn = static_cast<int>(it.t - first);
+                    sem = a.sems + (it.bi * g.h_q + it.h) * a.n_q_tiles + j;
+                    if (r == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (ld_acquire_gpu(sem) != turn) {
+                            if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+                                set_status(a.status, kStatusTimeout);
+                                *abort_flag = 1;
+                                break;
+                            }
+                        }
+                    }
+                    named_bar_sync(kBarDq, 128);
+                    turn_ok = *abort_flag == 0;
+                }
 #pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-            const uint32_t col = which == 0 ? tm_dv : tm_dk;
-            const float mul = which == 0 ? 1.f : a.scale;
-#pragma unroll 1
-            for (int ch = 0; ch < HD / 32; ++ch) {
-                uint32_t v[32];
-                if (has_work && ok) {
-                    tmem_ld32(col + lane_off + ch * 32, v);
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + C::kColDQ + lane_off + ch * 32, v);
                     tmem_ld_wait();
+                    if (row_ok && turn_ok) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            red_add_v4(dst + ch * 32 + e, __uint_as_float(v[e]) * a.scale,
+                                       __uint_as_float(v[e + 1]) * a.scale,
+                                       __uint_as_float(v[e + 2]) * a.scale,
+                                       __uint_as_float(v[e + 3]) * a.scale);
+                    }
                 }
-                float f[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] = live ? __uint_as_float(v[e]) * mul : 0.f;
-                if (!row_in_slot) continue;
-                if (a.dk_ws != nullptr) {
-                    float* dst = (which == 0 ? a.dv_ws : a.dk_ws) + (prow * g.h_q + h) * HD + ch * 32;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
-                } else {
-                    const int64_t* st = which == 0 ? a.dv_stride : a.dk_stride;
-                    uint16_t* base = static_cast<uint16_t*>(which == 0 ? a.dv : a.dk);
-                    uint16_t* dst = base + (g.layout == 1 ? prow * st[1] : bi * st[0] + kj * st[1]) +
-                                    gk * st[2] + ch * 32;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8)
-                        *reinterpret_cast<uint4*>(dst + e) =
-                            make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
-                                       pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
+                tc_fence_before();
+                mbar_arrive(bar(kDqEmpty));
+                if (a.deterministic) {
+                    __threadfence();
+                    named_bar_sync(kBarDq, 128);
+                    if (r == 0) st_release_gpu(sem, turn + 1);
                 }
             }
         }
     }
-    if (!ok && tid == 0) set_status(a.status, kStatusTimeout);
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -422,12 +612,16 @@ template <int HD, bool BF16>
 static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 {
     auto kern = sdpa_bwd_main_kernel<HD, BF16>;
-    const uint32_t bytes = Smem<HD>::kAlloc;
+    const uint32_t bytes = Cfg<HD>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     const int64_t items = a.g.b * a.g.h_q * a.n_kv_tiles;
     if (items == 0) return cudaSuccess;
-    kern<<<static_cast<unsigned>(items), kThreads, bytes, s>>>(a);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t grid = items < sms ? items : sms;
+    kern<<<static_cast<unsigned>(grid), kThreads, bytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace swa {
@@ -60,6 +61,9 @@ struct PreArgs {
 };
 
 struct MainArgs {
+    // TMA descriptors of Q, K, V, dO: BSHD 4-D (d, h, s, b), THD 3-D (d, h, t);
+    // 64 x 1 x 128 boxes with the 128-byte swizzle.
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
     Geometry g;
     const void *q, *k, *v, *dout;
     const float* lse;

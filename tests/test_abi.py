@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert "sdpa_bwd" in names and "sdpa_bwd_preprocess" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert set(names) <= set(swa.ENTRY_POINTS) | {"sdpa_bwd_no_alloc"}
+    assert set(names) <= set(swa.ENTRY_POINTS)
 
 
 def test_params_struct_matches_binding(lib):
