@@ -164,6 +164,35 @@ sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace
  */
 sdpa_status_t sdpa_bwd_check_status(const void *workspace, void *stream);
 
+/*
+ * Whole backward without a caller-provided workspace. The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory: a plug-in whose host application owns all device memory and
+ * lends none, a latency-critical path that must not pay for cudaMalloc's
+ * implicit synchronisation, or a deployment that forbids allocation once it
+ * has started.
+ *
+ * It enqueues the same four stages as sdpa_bwd_preprocess, sdpa_bwd,
+ * sdpa_bwd_dq_convert and sdpa_bwd_gqa_reduce on `stream`, with their scratch
+ * in a fixed array of SDPA_BWD_NO_ALLOC_MAX_BYTES inside this library (static
+ * device memory that every GPU loading the library keeps until the process
+ * exits). It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Size limit: a problem whose sdpa_bwd_workspace_bytes() exceeds
+ *    SDPA_BWD_NO_ALLOC_MAX_BYTES is rejected with SDPA_ERR_WORKSPACE before
+ *    anything is enqueued; use the workspace entry points for it.
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address once; make that first call before any stream
+ *    capture.
+ *  - Sharing: every call on a device uses the same array and leaves its
+ *    contents behind; each call re-zeroes what must start at zero. Calls whose
+ *    work overlaps on the GPU (other streams, other threads) race on the array
+ *    and must be serialised by the caller.
+ *  - Device-side status (a relay wait that ran out) is not reported by this
+ *    entry point; host-side errors are, as for the other calls.
+ */
+#define SDPA_BWD_NO_ALLOC_MAX_BYTES ((size_t)32 << 20)
+sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params *params, void *stream);
+
 /* Message of the last host-side error on the calling thread ("" if none). */
 const char *sdpa_bwd_last_error(void);
 

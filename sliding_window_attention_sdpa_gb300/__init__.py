@@ -28,7 +28,7 @@ SDPA_MASK_NONE, SDPA_MASK_TOP_LEFT, SDPA_MASK_BOTTOM_RIGHT = 0, 1, 2
 ENTRY_POINTS = ("sdpa_bwd_workspace_bytes", "sdpa_bwd_preprocess", "sdpa_bwd",
                 "sdpa_bwd_dq_convert", "sdpa_bwd_gqa_reduce", "sdpa_bwd_check_status",
                 "sdpa_bwd_last_error", "sdpa_bwd_params_bytes", "sdpa_bwd_tile_kv",
-                "sdpa_bwd_tile_q")
+                "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -88,6 +88,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [P, vp, sz, vp]
             f.restype = st
+        lib.sdpa_bwd_no_alloc.argtypes = [P, vp]
+        lib.sdpa_bwd_no_alloc.restype = st
         lib.sdpa_bwd_check_status.argtypes = [vp, vp]
         lib.sdpa_bwd_check_status.restype = st
         lib.sdpa_bwd_last_error.argtypes = []
@@ -139,6 +141,16 @@ def sdpa_bwd_gqa_reduce(params, workspace: int, workspace_bytes: int, stream: in
 
 def sdpa_bwd_check_status(workspace: int, stream: int) -> int:
     return load().sdpa_bwd_check_status(workspace, stream)
+
+
+# Largest scratch (bytes) sdpa_bwd_no_alloc can serve; see include/sdpa_bwd.h.
+SDPA_BWD_NO_ALLOC_MAX_BYTES = 32 << 20
+
+
+def sdpa_bwd_no_alloc(params, stream: int) -> int:
+    """Whole backward with the library's own fixed scratch: for callers that
+    cannot allocate device memory (no workspace argument, no allocation)."""
+    return load().sdpa_bwd_no_alloc(ctypes.byref(params), stream)
 
 
 # ------------------------------------------------------------- torch helpers

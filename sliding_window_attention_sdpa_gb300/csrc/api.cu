@@ -415,6 +415,72 @@ sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
 
 const char* sdpa_bwd_last_error(void) { return g_last_error.c_str(); }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without a caller-provided workspace, for callers that cannot
+// allocate device memory (see sdpa_bwd_no_alloc in the header). Its scratch is
+// this fixed array; host code never uses the array's name as an address (on
+// the host it is only a stand-in): the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+namespace {
+
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[SDPA_BWD_NO_ALLOC_MAX_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+sdpa_status_t no_alloc_scratch(void** out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDPA_ERR_CUDA, "sdpa_bwd_no_alloc: no current CUDA device (%s)",
+                    cudaGetErrorString(e));
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(SDPA_ERR_UNSUPPORTED, "sdpa_bwd_no_alloc: device %d beyond the %d supported", dev,
+                    kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return fail(SDPA_ERR_CUDA, "sdpa_bwd_no_alloc: cannot resolve the scratch array on device %d (%s)",
+                        dev, cudaGetErrorString(e));
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return SDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params* p, void* stream)
+{
+    sdpa_status_t st = check_shape(p);
+    if (st != SDPA_OK) return st;
+    const size_t need = layout_of(p).total;
+    if (need > SDPA_BWD_NO_ALLOC_MAX_BYTES)
+        return fail(SDPA_ERR_WORKSPACE,
+                    "sdpa_bwd_no_alloc: this problem needs %zu bytes of scratch, more than the fixed "
+                    "%zu bytes this entry point owns; call the workspace entry points instead",
+                    need, static_cast<size_t>(SDPA_BWD_NO_ALLOC_MAX_BYTES));
+    void* ws = nullptr;
+    if ((st = no_alloc_scratch(&ws)) != SDPA_OK) return st;
+    const size_t n = SDPA_BWD_NO_ALLOC_MAX_BYTES;
+    if ((st = sdpa_bwd_preprocess(p, ws, n, stream)) != SDPA_OK) return st;
+    if ((st = sdpa_bwd(p, ws, n, stream)) != SDPA_OK) return st;
+    if ((st = sdpa_bwd_dq_convert(p, ws, n, stream)) != SDPA_OK) return st;
+    return sdpa_bwd_gqa_reduce(p, ws, n, stream);
+}
+
 size_t sdpa_bwd_params_bytes(void) { return sizeof(sdpa_bwd_params); }
 
 int32_t sdpa_bwd_tile_kv(void) { return swa::kTileKV; }

@@ -1,0 +1,66 @@
+"""The allocation-free entry point, sdpa_bwd_no_alloc.
+
+It serves callers that cannot allocate device memory (a plug-in whose host
+application owns all device memory, a latency-critical path that must avoid
+cudaMalloc's synchronisation, a deployment that forbids allocation after
+start-up): it runs the whole backward with a fixed scratch array inside the
+library instead of a caller-provided workspace. These tests check, through the
+C ABI, that two calls in a row give the same gradients as the workspace entry
+points (within the bf16 tolerance of the other parity tests), and that a
+problem too large for the fixed scratch is refused on the host.
+
+This file is named to be collected last, so that a run stopping at the first
+failure has already run every other test.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import sliding_window_attention_sdpa_gb300 as swa
+from swa_cases import Case, build, compare
+
+
+def test_oversized_problem_is_refused_on_the_host():
+    swa._build.build()
+    p = swa.SdpaBwdParams()
+    p.dtype, p.layout, p.mask_mode = swa.SDPA_BF16, swa.SDPA_BSHD, swa.SDPA_MASK_TOP_LEFT
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 2, 16, 16, 8192, 8192, 64
+    p.window_left, p.window_right, p.scale = 128, -1, 0.125
+    need = swa.sdpa_bwd_workspace_bytes(p)
+    assert need > swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+    assert swa.sdpa_bwd_no_alloc(p, None) == swa.SDPA_ERR_WORKSPACE
+    msg = swa.last_error()
+    assert str(need) in msg and str(swa.SDPA_BWD_NO_ALLOC_MAX_BYTES) in msg
+
+
+@pytest.mark.gpu
+def test_no_alloc_matches_workspace_entry_points_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    swa.load()
+    # GQA + sink + padding so that every part of the scratch is in use
+    case = Case("no_alloc_gqa_sink", 2, 4, 2, 300, 300, 64, "tl", 64, lens_q=[300, 211],
+                lens_kv=[300, 211], sink=True, seed=31)
+    bt = build(case)
+    d = bt.dev
+    ref = swa.backward(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], check_status=True,
+                       **bt.kwargs)
+    torch.cuda.synchronize()
+    want = [t.double().cpu().numpy() for t in ref]
+
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        dq, dk, dv = (torch.full_like(d[n], float("nan")) for n in ("q", "k", "v"))
+        dsink = torch.full((case.h_q,), float("nan"), dtype=torch.float32, device=d["q"].device)
+        kw = dict(bt.kwargs)
+        sink = kw.pop("sink")
+        p = swa.make_params(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], dq, dk, dv,
+                            sink=sink, dsink=dsink, **kw)
+        assert swa.sdpa_bwd_workspace_bytes(p) <= swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+        rc = swa.sdpa_bwd_no_alloc(p, stream)
+        assert rc == swa.SDPA_OK, swa.last_error()
+        torch.cuda.synchronize()
+        for name, got, w in zip(("dq", "dk", "dv", "dsink"), (dq, dk, dv, dsink), want):
+            compare(f"call {call} {name}", got, w, case.dtype)
