@@ -116,43 +116,53 @@ typedef struct sdpa_bwd_params {
 /*
  * Workspace size in bytes for `params` (0 on invalid params; see
  * sdpa_bwd_last_error). The workspace holds the fp32 dQ accumulator, D = rowsum
- * (dO*O), the relay counters, the per-q-head fp32 dK/dV partials when
- * h_q != h_kv, the dSink partials and the status word. It must be 256-byte
+ * (dO*O), the relay counters, the dSink partials and the status word. It must be 256-byte
  * aligned device memory; its contents need no initialisation.
  */
 size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params *params);
 
 /*
  * Preprocess ("dot" kernel of PR #557's four-kernel split; delta of its dSink
- * formula): D[b,h,i] = sum_d dO*O in fp32 for every row, zeroes the fp32 dQ
- * accumulator, the relay counters and the status word, and writes the dSink
- * partials -exp(sink_h - LSE_i) * D_i summed over each block of unpadded rows.
+ * formula): D[b,h,i] = sum_d dO*O in fp32 for every row; zeroes the per-q-tile
+ * relay counters, the status word and (non-deterministic mode) the fp32 dQ
+ * accumulator rows of q-tiles that three or more kv-tiles visit; writes the
+ * dSink partials -exp(sink_h - LSE_i) * D_i summed over each block of 64
+ * unpadded rows.
  */
 sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params *params, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
 /*
- * Main backward ("main" kernel; PR #866 clamp and relay): one CTA per
- * (kv-tile, q-head, batch). Recomputes P and dS for each q-tile in the
- * clamped range [q_lo, q_hi) and accumulates dV, dK in tensor memory; adds
- * scale * dS K into the fp32 dQ accumulator (atomics, or in deterministic mode
- * the relay whose turn counts from kv_first = max((q_row0 + diag - W) //
- * tile_kv, 0)); stores dK, dV (h_q == h_kv) or fp32 per-q-head partials.
+ * Main backward ("main" kernel; PR #866 clamp and relay): one work item per
+ * (kv-tile, kv-head, batch). For each q-head of the kv-head's group and each
+ * q-tile in the clamped range [q_lo, q_hi) (swept from the top down) it
+ * recomputes P and dS and accumulates dV, dK in tensor memory, so the GQA/MQA
+ * group sum (PR #557) happens in place, in head order; stores dK, dV.
+ * dQ = scale * dS K of a q-tile is combined over the contiguous kv-tiles that
+ * visit it, [kv_first, kv_first + n) with kv_first = max((q_row0 + diag - W)
+ * // tile_kv, 0): a lone visitor stores dQ directly; in deterministic mode,
+ * or with two visitors, the tile passes along the relay (turn t - kv_first)
+ * through the fp32 accumulator and the last turn stores dQ; otherwise the
+ * visitors add with fp32 atomics and sdpa_bwd_dq_convert stores dQ.
  */
 sdpa_status_t sdpa_bwd(const sdpa_bwd_params *params, void *workspace, size_t workspace_bytes,
                        void *stream);
 
 /*
- * dQ convert ("cvt" kernel): dQ = dtype(fp32 accumulator), zero on padded rows,
- * and dsink[h] = fixed-order sum of the dSink partials (when a sink is used).
+ * dQ convert ("cvt" kernel): dQ = dtype(fp32 accumulator) on the q-tiles that
+ * took unordered atomics, dQ = 0 on rows no kv-tile visits (padding, gap
+ * tokens, rows outside every window), and dsink[h] = fixed-order sum of the
+ * dSink partials (when a sink is used).
  */
 sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params *params, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
 /*
- * GQA reduction ("reduce" kernel, PR #557 GQA/MQA): dK[., g] and dV[., g] are
- * the sums over the q-heads of group g of the per-q-head partials, in head
- * order. Returns SDPA_OK without enqueuing anything when h_q == h_kv.
+ * GQA reduction ("reduce" step, PR #557 GQA/MQA): dK[., g] and dV[., g] are
+ * sums over the q-heads of group g. sdpa_bwd already forms these sums in
+ * tensor memory (in head order), so this call only validates its arguments and
+ * enqueues nothing; it is kept so that the four-call sequence is the same for
+ * every head layout.
  */
 sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace,
                                   size_t workspace_bytes, void *stream);

@@ -117,10 +117,10 @@ int64_t rows_kv(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->to
 swa::WsLayout layout_of(const sdpa_bwd_params* p)
 {
     swa::WsLayout w{};
-    const int64_t rq = rows_q(p), rkv = rows_kv(p);
+    const int64_t rq = rows_q(p);
     const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
     w.n_sems = p->b * p->h_q * nqt;
-    w.n_row_blocks = (rq + swa::kPreRows - 1) / swa::kPreRows;
+    w.n_row_blocks = p->b * ((p->s_q + swa::kPreRows - 1) / swa::kPreRows);
     size_t off = 0;
     w.status = off;
     off = align256(off + 16);
@@ -132,14 +132,6 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     off = align256(off + static_cast<size_t>(w.n_sems) * 4);
     w.dsink_part = off;
     if (p->sink != nullptr) off = align256(off + static_cast<size_t>(p->h_q) * w.n_row_blocks * 4);
-    w.dk_ws = w.dv_ws = off;
-    if (p->h_q != p->h_kv) {
-        const size_t part = static_cast<size_t>(rkv) * p->h_q * p->d * 4;
-        w.dk_ws = off;
-        off = align256(off + part);
-        w.dv_ws = off;
-        off = align256(off + part);
-    }
     w.total = off;
     return w;
 }
@@ -290,6 +282,7 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
     copy3(a.o_stride, p->o_stride);
     copy3(a.do_stride, p->do_stride);
     a.dq_acc = at<float>(ws, w.dq_acc);
+    a.deterministic = p->deterministic;
     a.delta = at<float>(ws, w.delta);
     a.status = at<int32_t>(ws, w.status);
     a.sems = at<int32_t>(ws, w.sems);
@@ -321,12 +314,10 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     a.lse = p->lse;
     a.delta = at<float>(ws, w.delta);
     a.dq_acc = at<float>(ws, w.dq_acc);
+    a.dq = p->dq;
+    copy3(a.dq_stride, p->dq_stride);
     a.dk = p->dk;
     a.dv = p->dv;
-    if (p->h_q != p->h_kv) {
-        a.dk_ws = at<float>(ws, w.dk_ws);
-        a.dv_ws = at<float>(ws, w.dv_ws);
-    }
     a.status = at<int32_t>(ws, w.status);
     a.sems = at<int32_t>(ws, w.sems);
     copy3(a.q_stride, p->q_stride);
@@ -369,6 +360,7 @@ sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_
     swa::CvtArgs a{};
     a.g = geometry_of(p);
     a.dq_acc = at<float>(ws, w.dq_acc);
+    a.deterministic = p->deterministic;
     a.dq = p->dq;
     copy3(a.dq_stride, p->dq_stride);
     a.dsink_part = p->sink ? at<float>(ws, w.dsink_part) : nullptr;
@@ -381,20 +373,11 @@ sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_
 
 sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void* stream)
 {
-    sdpa_status_t st = check_all(p, ws, ws_bytes);
-    if (st != SDPA_OK) return st;
-    if (p->h_q == p->h_kv) return SDPA_OK;
-    const swa::WsLayout w = layout_of(p);
-    swa::ReduceArgs a{};
-    a.g = geometry_of(p);
-    a.dk_ws = at<float>(ws, w.dk_ws);
-    a.dv_ws = at<float>(ws, w.dv_ws);
-    a.dk = p->dk;
-    a.dv = p->dv;
-    copy3(a.dk_stride, p->dk_stride);
-    copy3(a.dv_stride, p->dv_stride);
-    return cuda_status(swa::launch_gqa_reduce(a, p->dtype, static_cast<cudaStream_t>(stream)),
-                       "gqa_reduce launch");
+    // The group sum of dK/dV happens inside sdpa_bwd (TMEM accumulation over
+    // the group's q-heads, in head order); this call only checks its arguments
+    // so that the four-call sequence stays the same for every head layout.
+    (void)stream;
+    return check_all(p, ws, ws_bytes);
 }
 
 sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)

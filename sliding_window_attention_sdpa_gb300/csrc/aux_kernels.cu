@@ -1,10 +1,11 @@
-// aux_kernels.cu -- the three HBM-bound kernels around the main backward:
-//  * preprocess ("dot"): D = rowsum(dO * O) in fp32, zero the fp32 dQ
-//    accumulator / relay counters / status, dSink partials;
-//  * dq_convert ("cvt"): fp32 dQ accumulator -> I/O dtype, dSink finish;
-//  * gqa_reduce ("reduce"): per-q-head fp32 dK/dV partials summed over each
-//    kv-head's group in head order -> I/O dtype.
-// All three move 16-byte vectors per thread with consecutive threads on
+// aux_kernels.cu -- the two HBM-bound kernels around the main backward:
+//  * preprocess ("dot"): D = rowsum(dO * O) in fp32, zero the relay / visit
+//    counters and the status word, dSink partials;
+//  * dq_convert ("cvt"): the main kernel already stored dQ (converted by each
+//    q-tile's last visitor); this writes dQ = 0 on the rows no kv-tile visits
+//    (padding, gap tokens, rows outside every window), converts the q-tiles
+//    that took unordered atomics, and finishes dSink.
+// Both move 16-byte vectors per thread with consecutive threads on
 // consecutive 16-byte pieces of a row, so every warp access is coalesced.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,8 +53,8 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 }
 
 // ---------------------------------------------------------------- preprocess
-// grid (n_row_blocks, h_q), 256 threads. Each row of HD features is read by
-// HD/8 consecutive threads (16 B each).
+// grid (ceil(s_q / 64), h_q, b): 64 rows of one sequence's slot for one q-head.
+// Each row of HD features is read by HD/8 consecutive threads (16 B each).
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
 {
@@ -62,54 +63,70 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
     const int c = tid % TPR;
-    const int64_t h = blockIdx.y;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRows;
+    const int64_t h = blockIdx.y, bi = blockIdx.z;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kPreRows;
     const bool with_sink = a.sink != nullptr;
-    const float sink = with_sink ? a.sink[h] : 0.f;
-    float dsink_acc = 0.f;
 
-    // relay counters, ticket and status: zeroed by the whole grid
+    // relay / visit counters, ticket and status: zeroed by the whole grid
     {
-        const int64_t nthr = static_cast<int64_t>(gridDim.x) * gridDim.y * blockDim.x;
-        const int64_t id = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + tid;
+        const int64_t nthr = static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z * blockDim.x;
+        const int64_t id = ((static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x +
+                            blockIdx.x) * blockDim.x + tid;
         for (int64_t k = id; k < a.n_sems; k += nthr) a.sems[k] = 0;
         if (id == 0) {
             a.status[0] = 0;
             a.status[1] = 0;
         }
     }
+    const SeqInfo s = seq_info(g, bi);
+    const int64_t blk = bi * gridDim.x + blockIdx.x;  // dSink partial slot
+    if (i0 >= s.slot_q) {
+        if (with_sink && tid == 0) a.dsink_part[h * a.n_row_blocks + blk] = 0.f;
+        return;
+    }
+    const float sink = with_sink ? a.sink[h] : 0.f;
+    // q-tiles with three or more visitors take unordered atomics (unless
+    // deterministic): their accumulator rows start at zero
+    bool zero_acc = false;
+    if (!a.deterministic && i0 < s.len_q) {
+        int64_t first, n;
+        q_tile_visitors(g, s, i0 / kTileQ, first, n);
+        zero_acc = n >= 3;
+    }
+    const uint16_t* o = static_cast<const uint16_t*>(a.o);
+    const uint16_t* dout = static_cast<const uint16_t*>(a.dout);
+    const bool thd = g.layout == 1;
+    float dsink_acc = 0.f;
 
-#pragma unroll 1
+#pragma unroll 2
     for (int r = tid / TPR; r < kPreRows; r += RPP) {
-        const int64_t row = row0 + r;
-        const bool in_range = row < g.rows_q;
+        const int64_t i = i0 + r;
+        const bool in_slot = i < s.slot_q;
+        const bool valid = i < s.len_q;
         float part = 0.f;
-        bool valid = false;
-        int64_t stat = 0;
-        if (in_range) {
-            const int64_t bi = q_row_seq(g, row);
-            const SeqInfo s = seq_info(g, bi);
-            valid = (row - s.q_row0) < s.len_q;
-            stat = stat_offset(g, row, h);
-            if (valid) {
-                const int64_t oo = elem_offset(g, a.o_stride, row, g.s_q, h) + c * 8;
-                const int64_t od = elem_offset(g, a.do_stride, row, g.s_q, h) + c * 8;
-                float fo[8], fd[8];
-                unpack8<BF16>(ld_nc_v4(static_cast<const uint16_t*>(a.o) + oo), fo);
-                unpack8<BF16>(ld_nc_v4(static_cast<const uint16_t*>(a.dout) + od), fd);
+        if (valid) {
+            const int64_t oo = (thd ? (s.q_row0 + i) * a.o_stride[1] : bi * a.o_stride[0] + i * a.o_stride[1]) +
+                               h * a.o_stride[2] + c * 8;
+            const int64_t od = (thd ? (s.q_row0 + i) * a.do_stride[1] : bi * a.do_stride[0] + i * a.do_stride[1]) +
+                               h * a.do_stride[2] + c * 8;
+            float fo[8], fd[8];
+            unpack8<BF16>(ld_nc_v4(o + oo), fo);
+            unpack8<BF16>(ld_nc_v4(dout + od), fd);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) part = fmaf(fo[e], fd[e], part);
-            }
-            float4* acc = reinterpret_cast<float4*>(a.dq_acc + (row * g.h_q + h) * HD + c * 8);
-            acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < 8; ++e) part = fmaf(fo[e], fd[e], part);
+        }
+        if (zero_acc && valid) {
+            float4* z = reinterpret_cast<float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (in_range && c == 0) {
-            a.delta[stat] = valid ? part : 0.f;
+        if (in_slot && c == 0) {
+            const int64_t so = thd ? h * g.rows_q + s.q_row0 + i : (bi * g.h_q + h) * g.s_q + i;
+            a.delta[so] = valid ? part : 0.f;
             if (with_sink && valid) {
-                const float lse = a.lse[stat];
+                const float lse = a.lse[so];
                 if (lse != -INFINITY) dsink_acc -= expf(sink - lse) * part;
             }
         }
@@ -122,14 +139,18 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
         if ((tid & 31) == 0) red[tid >> 5] = dsink_acc;
         __syncthreads();
         if (tid == 0) {
-            float s = 0.f;
-            for (int w = 0; w < 8; ++w) s += red[w];
-            a.dsink_part[h * a.n_row_blocks + blockIdx.x] = s;
+            float t = 0.f;
+            for (int w = 0; w < 8; ++w) t += red[w];
+            a.dsink_part[h * a.n_row_blocks + blk] = t;
         }
     }
 }
 
 // ---------------------------------------------------------------- convert
+// The main kernel already stored dQ for every q-tile some kv-tile visits (its
+// last visitor converts). This writes dQ = 0 on the other rows of a slot:
+// rows past the sequence's length and q-tiles no kv-tile visits. grid
+// (ceil(s_q / 128), h_q, b). It also finishes dSink in a fixed order.
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
 {
@@ -138,59 +159,48 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
     const int c = tid % TPR;
-    const int64_t h = blockIdx.y;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRows;
-#pragma unroll 1
-    for (int r = tid / TPR; r < kPreRows; r += RPP) {
-        const int64_t row = row0 + r;
-        if (row >= g.rows_q) break;
-        const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (row * g.h_q + h) * HD + c * 8);
-        const float4 x = src[0], y = src[1];
-        const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-        uint16_t* dst = static_cast<uint16_t*>(a.dq) + elem_offset(g, a.dq_stride, row, g.s_q, h) + c * 8;
-        *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
-    }
-    if (a.dsink != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
+    const int64_t j = blockIdx.x, h = blockIdx.y, bi = blockIdx.z;
+    if (a.dsink != nullptr && j == 0 && h == 0 && bi == 0) {
         // fixed-order finish: bitwise repeatable
         for (int64_t hh = tid; hh < g.h_q; hh += blockDim.x) {
-            float s = 0.f;
-            for (int64_t k = 0; k < a.n_row_blocks; ++k) s += a.dsink_part[hh * a.n_row_blocks + k];
-            a.dsink[hh] = s;
+            float t = 0.f;
+            for (int64_t k = 0; k < a.n_row_blocks; ++k) t += a.dsink_part[hh * a.n_row_blocks + k];
+            a.dsink[hh] = t;
         }
     }
-}
-
-// ---------------------------------------------------------------- GQA reduce
-template <int HD, bool BF16>
-__global__ void __launch_bounds__(256) gqa_reduce_kernel(const ReduceArgs a)
-{
-    constexpr int TPR = HD / 8;
-    constexpr int RPP = 256 / TPR;
-    const Geometry& g = a.g;
-    const int tid = threadIdx.x;
-    const int c = tid % TPR;
-    const int64_t gk = blockIdx.y;
-    const int64_t group = g.h_q / g.h_kv;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRows;
+    const SeqInfo s = seq_info(g, bi);
+    const int64_t t0 = j * kTileQ;
+    const int64_t t1 = imin(t0 + kTileQ, s.slot_q);
+    if (t0 >= t1) return;
+    int64_t z0 = t0;  // first row to zero
+    bool accumulated = false;
+    if (t0 < s.len_q) {
+        int64_t first, n;
+        q_tile_visitors(g, s, j, first, n);
+        if (n > 0) z0 = s.len_q;
+        accumulated = n >= 3 && !a.deterministic;
+    }
+    const bool thd = g.layout == 1;
+    uint16_t* dq = static_cast<uint16_t*>(a.dq);
+    if (accumulated) {
+        // rows whose dQ was summed with unordered atomics: convert them
+        const int64_t e1 = imin(t1, s.len_q);
 #pragma unroll 1
-    for (int r = tid / TPR; r < kPreRows; r += RPP) {
-        const int64_t row = row0 + r;
-        if (row >= g.rows_kv) break;
-        float sk[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int64_t hh = gk * group; hh < (gk + 1) * group; ++hh) {
-            const int64_t o = (row * g.h_q + hh) * HD + c * 8;
-            const float4* pk = reinterpret_cast<const float4*>(a.dk_ws + o);
-            const float4* pv = reinterpret_cast<const float4*>(a.dv_ws + o);
-            const float4 k0 = pk[0], k1 = pk[1], v0 = pv[0], v1 = pv[1];
-            sk[0] += k0.x; sk[1] += k0.y; sk[2] += k0.z; sk[3] += k0.w;
-            sk[4] += k1.x; sk[5] += k1.y; sk[6] += k1.z; sk[7] += k1.w;
-            sv[0] += v0.x; sv[1] += v0.y; sv[2] += v0.z; sv[3] += v0.w;
-            sv[4] += v1.x; sv[5] += v1.y; sv[6] += v1.z; sv[7] += v1.w;
+        for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
+            const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8);
+            const float4 x = src[0], y = src[1];
+            const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+            uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
+                            h * a.dq_stride[2] + c * 8;
+            *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
         }
-        uint16_t* dk = static_cast<uint16_t*>(a.dk) + elem_offset(g, a.dk_stride, row, g.s_kv, gk) + c * 8;
-        uint16_t* dv = static_cast<uint16_t*>(a.dv) + elem_offset(g, a.dv_stride, row, g.s_kv, gk) + c * 8;
-        *reinterpret_cast<uint4*>(dk) = pack8<BF16>(sk);
-        *reinterpret_cast<uint4*>(dv) = pack8<BF16>(sv);
+    }
+    if (z0 >= t1) return;
+#pragma unroll 1
+    for (int64_t i = z0 + tid / TPR; i < t1; i += RPP) {
+        uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
+                        h * a.dq_stride[2] + c * 8;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -206,26 +216,19 @@ __global__ void __launch_bounds__(256) gqa_reduce_kernel(const ReduceArgs a)
 
 cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
 {
-    if (a.n_row_blocks == 0 || a.g.h_q == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(a.n_row_blocks), static_cast<unsigned>(a.g.h_q));
+    const int64_t nx = (a.g.s_q + kPreRows - 1) / kPreRows;
+    if (nx == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>(nx), static_cast<unsigned>(a.g.h_q), static_cast<unsigned>(a.g.b));
     SWA_DISPATCH(preprocess_kernel, a, grid, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s)
 {
-    if (a.n_row_blocks == 0 || a.g.h_q == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(a.n_row_blocks), static_cast<unsigned>(a.g.h_q));
+    const int64_t nx = (a.g.s_q + kTileQ - 1) / kTileQ;
+    if (nx == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>(nx), static_cast<unsigned>(a.g.h_q), static_cast<unsigned>(a.g.b));
     SWA_DISPATCH(dq_convert_kernel, a, grid, s);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gqa_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
-{
-    const int64_t blocks = (a.g.rows_kv + kPreRows - 1) / kPreRows;
-    if (blocks == 0 || a.g.h_kv == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(a.g.h_kv));
-    SWA_DISPATCH(gqa_reduce_kernel, a, grid, s);
     return cudaGetLastError();
 }
 

@@ -1,28 +1,33 @@
 // main_kernel.cu -- fused sliding-window SDPA backward on sm_103a tensor cores.
 //
-// Work item = (kv-tile t, q-head h, sequence b). A persistent CTA (one per SM)
-// walks its items; for each it keeps the kv-tile's K and V in shared memory and
-// sweeps the q-tiles in the window-clamped range [q_lo, q_hi) (cuDNN-frontend
-// PR #866, "Change": no query with anchor > kv_base + tile_kv - 1 + W reaches
-// the tile), issuing the five contractions as tcgen05.mma with fp32
-// accumulators in tensor memory (TMEM):
+// Work item = (kv-tile t, kv-head g, sequence b). A persistent CTA (one per SM)
+// walks its items; for each it keeps the kv-tile's K and V in shared memory and,
+// for every q-head of g's group in turn, sweeps the q-tiles in the
+// window-clamped range [q_lo, q_hi) (cuDNN-frontend PR #866, "Change": no query
+// with anchor > kv_base + tile_kv - 1 + W reaches the tile) from the top down,
+// issuing the five contractions as tcgen05.mma with fp32 accumulators in tensor
+// memory (TMEM). dK and dV accumulate over the whole group in TMEM (the GQA
+// reduction of PR #557, in head order) and are stored once per item:
 //
 //   S^T  = K Q^T     [kv x q]  cols   0..127
 //   dP^T = V dO^T    [kv x q]  cols 128..255
-//   dV  += P^T dO    [kv x d]  cols 256..
+//   dV  += P^T dO    [kv x d]  cols 256..      (d = 64: P^T read from TMEM)
 //   dK  += dS^T Q    [kv x d]  cols 256+d..
 //   dQ   = dS K      [q x d]   cols 384.. (d = 64) or aliasing S^T (d = 128)
+//   P^T (16-bit)     [kv x q]  cols 448..511 (d = 64; two q per column)
 //
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0      TMA producer: K, V per item; Q, dO per q-tile into a ring of
 //               kStages stages (128-byte swizzle, zero fill past the tensor)
 //   warp 1      MMA issuer (one thread) and TMEM owner
 //   warps 2-3   LSE / D loader: the q-tile's 128 LSE (log2 domain) and D values
-//   warps 4-7   softmax: one thread per kv row (TMEM lane) recomputes
-//               P = exp2(S*scale*log2e - LSE*log2e) and dS = P (dP - D) with
-//               the mask, writes P^T / dS^T as swizzled 16-bit tiles; at the end
-//               of an item stores dK, dV (or fp32 GQA partials)
-//   warps 8-11  dQ: one thread per q row reads dQ from TMEM and adds it to the
+//   warps 4-11  softmax: two warps per TMEM sub-partition, each thread one kv
+//               row (TMEM lane) and one 64-column half of the q-tile; recomputes
+//               P = exp2(S*scale*log2e - LSE*log2e) and dS = P (dP - D) with the
+//               mask, skipping 32-column chunks the window masks for the whole
+//               warp; writes P^T / dS^T as swizzled 16-bit tiles; at the end of
+//               an item one half stores dV, the other dK (or fp32 GQA partials)
+//   warps 12-15 dQ: one thread per q row reads dQ from TMEM and adds it to the
 //               fp32 accumulator (vector atomics, or the ordered relay)
 // Hand-offs are mbarriers; every wait is bounded (status word on timeout).
 //
@@ -43,14 +48,15 @@ namespace swa {
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBlock16K = 128 * 128;  // one 64-column block of a 128-row tile
 constexpr float kLog2e = 1.4426950408889634f;
 
 // warp roles
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLse0 = 2, kWarpSoft0 = 4, kWarpDq0 = 8;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLse0 = 2, kWarpSoft0 = 4, kWarpDq0 = 12;
 constexpr int kLseThreads = 64;
+constexpr int kSoftThreads = 256;
 constexpr int kBarDq = 1, kBarSoft = 2;  // named barriers of the two 128-thread groups
 
 template <int HD>
@@ -63,8 +69,9 @@ struct Cfg {
     static constexpr uint32_t kV = kK + kKvStages * kTile;      // kKvStages tiles
     static constexpr uint32_t kQ = kV + kKvStages * kTile;      // kStages tiles
     static constexpr uint32_t kDO = kQ + kStages * kTile;       // kStages tiles
-    static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q]
-    static constexpr uint32_t kDS = kP + 32768;                 // dS^T [128 kv x 128 q]
+    static constexpr bool kPInTmem = HD == 64;                  // P^T kept in TMEM
+    static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q] (d = 128)
+    static constexpr uint32_t kDS = kP + (kPInTmem ? 0 : 32768); // dS^T [128 kv x 128 q]
     static constexpr uint32_t kLse = kDS + 32768;               // kStages x 128 fp32
     static constexpr uint32_t kDelta = kLse + kStages * 512;    // kStages x 128 fp32
     static constexpr uint32_t kBars = kDelta + kStages * 512;   // mbarriers
@@ -74,6 +81,7 @@ struct Cfg {
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
     static constexpr uint32_t kColDQ = HD == 64 ? 384 : 0;
+    static constexpr uint32_t kColP = 448;                      // d = 64 only
     static constexpr bool kDqAliasesS = HD != 64;
 };
 
@@ -153,36 +161,34 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool v)
     return r != 0;
 }
 
-// q-tile range [lo, hi) of kv rows [kv_base, kv_end) of one sequence: lo is
-// the first q-tile holding a row that reaches key kv_base (right bound), hi
-// the clamp ceil((kv_end + W - diag) / tile_q) (left window).
-__device__ __forceinline__ void q_range(const Geometry& g, const SeqInfo& s, int64_t kv_base,
-                                        int64_t kv_end, int64_t& lo, int64_t& hi)
-{
-    const int64_t n_q = (s.len_q + kTileQ - 1) / kTileQ;
-    lo = 0;
-    hi = n_q;
-    if (kv_base >= s.len_kv || n_q == 0) {
-        hi = 0;
-        return;
-    }
-    if (g.right >= 0) {
-        const int64_t first = kv_base - g.right - s.diag;
-        lo = first > 0 ? first / kTileQ : 0;
-    }
-    if (g.window_left >= 0) {
-        const int64_t c = floor_div(kv_end + g.window_left - s.diag + kTileQ - 1, kTileQ);
-        if (c < hi) hi = c;
-    }
-    if (hi < lo) hi = lo;
-}
+// Optional timeline trace (build with -DSDPA_BWD_TRACE): SM clock stamps of each
+// role's hand-offs for the first kTraceCtas CTAs and kTraceTiles q-tiles, written
+// to the workspace at byte offset kTraceOffset (the caller sizes the workspace
+// for it). Off by default; it records and changes nothing else.
+constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceSlots = 16;
+constexpr size_t kTraceOffset = size_t(256) << 20;
+#ifdef SDPA_BWD_TRACE
+#define SWA_TRACE(slot, tile)                                                                    \
+    do {                                                                                         \
+        if (blockIdx.x < kTraceCtas && (tile) < kTraceTiles)                                     \
+            reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(a.status) + kTraceOffset)       \
+                [(blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (slot)] = clock64();         \
+    } while (0)
+#else
+#define SWA_TRACE(slot, tile) do { } while (0)
+#endif
 
 struct Item {
-    int64_t t, h, bi, gk;
+    int64_t t, bi, gk;
+    int64_t h0, group;   // q-heads [h0, h0 + group) share kv-head gk
     SeqInfo s;
     int64_t kv_base, q_lo, q_hi;
-    bool has_work;   // at least one q-tile to sweep
-    bool in_slot;    // the kv-tile has rows inside the sequence's slot
+    int64_t nq, steps;   // q-tiles per head, steps = group * nq
+    bool has_work;       // at least one q-tile to sweep
+    bool in_slot;        // the kv-tile has rows inside the sequence's slot
+    // step k: q-head h0 + k / nq, q-tile q_hi - 1 - k % nq
+    __device__ __forceinline__ int64_t head(int64_t k) const { return h0 + k / nq; }
+    __device__ __forceinline__ int64_t qtile(int64_t k) const { return q_hi - 1 - k % nq; }
 };
 
 __device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
@@ -190,15 +196,17 @@ __device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
     const Geometry& g = a.g;
     Item it;
     it.t = item % a.n_kv_tiles;
-    it.h = (item / a.n_kv_tiles) % g.h_q;
-    it.bi = item / (a.n_kv_tiles * g.h_q);
-    it.gk = it.h / (g.h_q / g.h_kv);
+    it.gk = (item / a.n_kv_tiles) % g.h_kv;
+    it.bi = item / (a.n_kv_tiles * g.h_kv);
+    it.group = g.h_q / g.h_kv;
+    it.h0 = it.gk * it.group;
     it.s = seq_info(g, it.bi);
     it.kv_base = it.t * kTileKV;
-    const int64_t kv_end = imin(it.kv_base + kTileKV, it.s.len_kv);
-    q_range(g, it.s, it.kv_base, kv_end, it.q_lo, it.q_hi);
+    q_tile_range(g, it.s, it.t, it.q_lo, it.q_hi);
+    it.nq = it.q_hi - it.q_lo;
+    it.steps = it.nq > 0 ? it.nq * it.group : 0;
     it.in_slot = it.kv_base < it.s.slot_kv;
-    it.has_work = it.q_hi > it.q_lo && it.in_slot;
+    it.has_work = it.nq > 0 && it.in_slot;
     return it;
 }
 
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint64_t tmo = static_cast<uint64_t>(a.timeout_ns);
-    const int64_t n_items = g.b * g.h_q * a.n_kv_tiles;
+    const int64_t n_items = g.b * g.h_kv * a.n_kv_tiles;
     const bool thd = g.layout == 1;
 
     if (tid == 0) {
@@ -249,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             mbar_init(bar(kKvEmpty0 + s), 1);
         }
         mbar_init(bar(kSFull), 1);
-        mbar_init(bar(kPFull), 128);
+        mbar_init(bar(kPFull), kSoftThreads);
         mbar_init(bar(kDqFull), 1);
         mbar_init(bar(kDqEmpty), 128);
         mbar_init(bar(kAccFull), 1);
-        mbar_init(bar(kAccEmpty), 128);
+        mbar_init(bar(kAccEmpty), kSoftThreads);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(kQFull0 + s), 1 + kLseThreads);
             mbar_init(bar(kQEmpty0 + s), 1);
@@ -282,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     auto wait_warp = [&](int b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, wait(b, parity));
     };
-    auto wait_group = [&](int id, int b, uint32_t parity) -> bool {
-        return bar_and(id, 128, wait(b, parity));
+    auto wait_group = [&](int id, int count, int b, uint32_t parity) -> bool {
+        return bar_and(id, count, wait(b, parity));
     };
 
     if (warp == kWarpTma) {
@@ -303,15 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 tma_tile<HD>(sbase + C::kV + ks * C::kTile, &a.tm_v, bar(kKvFull0 + ks), thd,
                              (int)it.gk, kvrow, (int)it.bi);
                 bool ok = true;
-                for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
+                    const int64_t j = it.qtile(k), hh = it.head(k);
                     const int st = q_it % C::kStages;
                     if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
+                    SWA_TRACE(12, q_it);
                     const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
                     mbar_arrive_expect_tx(bar(kQFull0 + st), 2 * C::kTile);
                     tma_tile<HD>(sbase + C::kQ + st * C::kTile, &a.tm_q, bar(kQFull0 + st), thd,
-                                 (int)it.h, qrow, (int)it.bi);
+                                 (int)hh, qrow, (int)it.bi);
                     tma_tile<HD>(sbase + C::kDO + st * C::kTile, &a.tm_do, bar(kQFull0 + st), thd,
-                                 (int)it.h, qrow, (int)it.bi);
+                                 (int)hh, qrow, (int)it.bi);
+                    SWA_TRACE(13, q_it);
                 }
                 if (!ok) break;
             }
@@ -334,9 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             const uint32_t sK = sbase + C::kK + ks * C::kTile, sV = sbase + C::kV + ks * C::kTile;
             if (it.kv_base + kTileKV > it.s.len_kv)
                 zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
-            for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+            for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
+                const int64_t j = it.qtile(k);
                 const int st = q_it % C::kStages;
                 if (!(ok = wait_warp(kQFull0 + st, (q_it / C::kStages) & 1))) break;
+                if (lane == 0) SWA_TRACE(0, q_it);
                 const int64_t q0 = j * kTileQ;
                 if (q0 + kTileQ > it.s.len_q) {
                     zero_tail<HD>(sm + C::kQ + st * C::kTile, it.s.len_q - q0, lane);
@@ -360,22 +373,30 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                     sdesc_sw128(sDO + koff, 16, 1024), kIdQK, k > 0);
                     }
                     umma_commit(bar(kSFull));
+                    SWA_TRACE(1, q_it);
                 }
                 __syncwarp();
                 // P^T, dS^T ready in shared memory (softmax done with S^T, dP^T)
                 if (!(ok = wait_warp(kPFull, p_it & 1))) break;
+                if (lane == 0) SWA_TRACE(2, q_it);
                 ++p_it;
                 if (!C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
-                if (j == it.q_lo && !(ok = wait_warp(kAccEmpty, (acc_it & 1) ^ 1))) break;
+                if (k == 0 && !(ok = wait_warp(kAccEmpty, (acc_it & 1) ^ 1))) break;
                 ++dq_it;
                 if (lane == 0) {
+                    SWA_TRACE(3, q_it);
                     tc_fence_after();
-                    const uint32_t acc = j > it.q_lo ? 1u : 0u;
+                    const uint32_t acc = k > 0 ? 1u : 0u;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024),
-                                    sdesc_sw128(sDO + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
+                        const uint64_t bdesc = sdesc_sw128(sDO + k * 2048, kBlock16K, 1024);
+                        if constexpr (C::kPInTmem) {
+                            umma_f16_ts(tm_dv, tmem + C::kColP + k * 8, bdesc, kIdPV, acc | (k > 0));
+                        } else {
+                            const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                            umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), bdesc, kIdPV,
+                                        acc | (k > 0));
+                        }
                     }
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -389,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                     sdesc_sw128(sK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
                     umma_commit(bar(kDqFull));
                     umma_commit(bar(kQEmpty0 + st));
-                    if (j + 1 == it.q_hi) {
+                    SWA_TRACE(4, q_it);
+                    if (k + 1 == it.steps) {
                         umma_commit(bar(kAccFull));
                         umma_commit(bar(kKvEmpty0 + ks));
                     }
@@ -407,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode(a, item);
             if (!it.has_work) continue;
-            for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+            for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
+                const int64_t j = it.qtile(k), hh = it.head(k);
                 const int st = q_it % C::kStages;
                 if (!(ok = wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1))) break;
                 float* sl = reinterpret_cast<float*>(sm + C::kLse + st * 512);
@@ -417,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     const int64_t qi = j * kTileQ + r;
                     float lse = INFINITY, dlt = 0.f;
                     if (qi < it.s.len_q) {
-                        const int64_t so = stat_offset(g, it.s.q_row0 + qi, it.h);
+                        const int64_t so = stat_offset(g, it.s.q_row0 + qi, hh);
                         lse = a.lse[so];
                         dlt = a.delta[so];
                         if (lse == -INFINITY) lse = INFINITY;  // row attends nothing: P = 0
@@ -426,106 +449,134 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     sd[r] = dlt;
                 }
                 mbar_arrive(bar(kQFull0 + st));
+                if (lt == 0) SWA_TRACE(14, q_it);
             }
         }
     } else if (warp < kWarpDq0) {
         // ------------------------------------------------------------ softmax + dK/dV epilogue
-        const int r = tid - kWarpSoft0 * 32;  // kv row within the tile = TMEM lane
+        const int r = (warp & 3) * 32 + lane;        // kv row within the tile = TMEM lane
+        const int half = (warp - kWarpSoft0) >> 2;   // q columns [64 half, 64 half + 64)
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint32_t q_it = 0, s_it = 0, acc_it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
             const Item it = decode(a, item);
             const int64_t kj = it.kv_base + r;
-            if (r == 0 && it.s.bad && it.t == 0 && it.h == 0) set_status(a.status, kStatusBadLengths);
+            if (r == 0 && half == 0 && it.s.bad && it.t == 0 && it.gk == 0)
+                set_status(a.status, kStatusBadLengths);
             if (it.has_work && ok) {
                 int64_t i_lo = 0, i_hi = it.s.len_q - 1;
                 if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - it.s.diag);
                 if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - it.s.diag);
                 if (kj >= it.s.len_kv) i_hi = -1;
-                for (int64_t j = it.q_lo; j < it.q_hi; ++j, ++q_it) {
+                for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
+                    const int64_t j = it.qtile(k);
                     const int st = q_it % C::kStages;
-                    if (!(ok = wait_group(kBarSoft, kQFull0 + st, (q_it / C::kStages) & 1))) break;
-                    if (!(ok = wait_group(kBarSoft, kSFull, s_it & 1))) break;
+                    if (!(ok = wait_group(kBarSoft, kSoftThreads, kQFull0 + st, (q_it / C::kStages) & 1))) break;
+                    if (!(ok = wait_group(kBarSoft, kSoftThreads, kSFull, s_it & 1))) break;
+                    if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                        SWA_TRACE(warp == kWarpSoft0 ? 5 : 7, q_it);
                     ++s_it;
                     tc_fence_after();
                     const float* sl = reinterpret_cast<const float*>(sm + C::kLse + st * 512);
                     const float* sd = reinterpret_cast<const float*>(sm + C::kDelta + st * 512);
                     const int64_t q0 = j * kTileQ;
-                    const int64_t c_lo = imax(i_lo - q0, 0);
-                    const int64_t c_hi = imin(i_hi - q0, 127);
+                    const int c_lo = static_cast<int>(imax(i_lo - q0, 0));
+                    const int c_hi = static_cast<int>(imin(i_hi - q0, 127));
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t sv[32], dpv[32];
-                        tmem_ld32(tmem + C::kColS + lane_off + ch * 32, sv);
-                        tmem_ld32(tmem + C::kColDP + lane_off + ch * 32, dpv);
-                        tmem_ld_wait();
-                        uint32_t pk[16], dk[16];
+                    for (int sc = 4 * half; sc < 4 * half + 4; ++sc) {
+                        const int c0 = sc * 16;
+                        // warp-uniform class of this 16-column chunk
+                        const bool none = __all_sync(0xffffffffu, c_hi < c0 || c_lo > c0 + 15);
+                        const bool full = __all_sync(0xffffffffu, c_lo <= c0 && c_hi >= c0 + 15);
+                        uint32_t pk[8], dk[8];
+                        if (none) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float p2[2], d2[2];
+                            for (int e = 0; e < 8; ++e) pk[e] = dk[e] = 0u;
+                        } else {
+                            uint32_t sv[16], dpv[16];
+                            tmem_ld16(tmem + C::kColS + lane_off + c0, sv);
+                            tmem_ld16(tmem + C::kColDP + lane_off + c0, dpv);
+                            tmem_ld_wait();
+                            if (full) {
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int c = ch * 32 + e + u;
-                                const bool att = c >= c_lo && c <= c_hi;
-                                const float p = att ? ex2_approx(fmaf(__uint_as_float(sv[e + u]),
-                                                                     a.scale_log2, -sl[c]))
-                                                    : 0.f;
-                                p2[u] = p;
-                                d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - sd[c]) : 0.f;
+                                for (int e = 0; e < 16; e += 2) {
+                                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -sl[c0 + e]));
+                                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -sl[c0 + e + 1]));
+                                    pk[e >> 1] = pack2<BF16>(p0, p1);
+                                    dk[e >> 1] = pack2<BF16>(p0 * (__uint_as_float(dpv[e]) - sd[c0 + e]),
+                                                             p1 * (__uint_as_float(dpv[e + 1]) - sd[c0 + e + 1]));
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; e += 2) {
+                                    float p2[2], d2[2];
+#pragma unroll
+                                    for (int u = 0; u < 2; ++u) {
+                                        const int c = c0 + e + u;
+                                        const bool att = c >= c_lo && c <= c_hi;
+                                        const float p = att ? ex2_approx(fmaf(__uint_as_float(sv[e + u]),
+                                                                             a.scale_log2, -sl[c]))
+                                                            : 0.f;
+                                        p2[u] = p;
+                                        d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - sd[c]) : 0.f;
+                                    }
+                                    pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
+                                    dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);
+                                }
                             }
-                            pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
-                            dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);
+                        }
+                        if constexpr (C::kPInTmem) {
+                            tmem_st8(tmem + C::kColP + lane_off + sc * 8, pk);
                         }
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t off = swz(r, ch * 4 + m);
-                            *reinterpret_cast<uint4*>(sm + C::kP + off) =
-                                make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
+                        for (int m = 0; m < 2; ++m) {
+                            const uint32_t off = swz(r, sc * 2 + m);
+                            if constexpr (!C::kPInTmem)
+                                *reinterpret_cast<uint4*>(sm + C::kP + off) =
+                                    make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                             *reinterpret_cast<uint4*>(sm + C::kDS + off) =
                                 make_uint4(dk[4 * m], dk[4 * m + 1], dk[4 * m + 2], dk[4 * m + 3]);
                         }
                     }
+                    if constexpr (C::kPInTmem) tmem_st_wait();
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(bar(kPFull));
+                    if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                        SWA_TRACE(warp == kWarpSoft0 ? 6 : 8, q_it);
                 }
-                if (ok) ok = wait_group(kBarSoft, kAccFull, acc_it & 1);
+                if (ok) ok = wait_group(kBarSoft, kSoftThreads, kAccFull, acc_it & 1);
                 ++acc_it;
                 if (ok) tc_fence_after();
             }
-            // epilogue: dV, dK (scaled) of this thread's kv row
+            // epilogue: half 0 stores this kv row's dV, half 1 its dK (scaled)
             if (!it.in_slot) continue;
             const bool live = it.has_work && ok && kj < it.s.len_kv;
             const bool row_in_slot = kj < it.s.slot_kv;
             const int64_t prow = it.s.kv_row0 + kj;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
+            const int which = half;
+            {
                 const uint32_t col = tmem + (which == 0 ? C::kColDV : C::kColDK);
                 const float mul = which == 0 ? 1.f : a.scale;
 #pragma unroll 1
-                for (int ch = 0; ch < HD / 32; ++ch) {
-                    uint32_t v[32];
+                for (int ch = 0; ch < HD / 16; ++ch) {
+                    uint32_t v[16];
                     if (it.has_work && ok) {
-                        tmem_ld32(col + lane_off + ch * 32, v);
+                        tmem_ld16(col + lane_off + ch * 16, v);
                         tmem_ld_wait();
                     }
-                    float f[32];
+                    float f[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) f[e] = live ? __uint_as_float(v[e]) * mul : 0.f;
+                    for (int e = 0; e < 16; ++e) f[e] = live ? __uint_as_float(v[e]) * mul : 0.f;
                     if (!row_in_slot) continue;
-                    if (a.dk_ws != nullptr) {
-                        float* dst = (which == 0 ? a.dv_ws : a.dk_ws) + (prow * g.h_q + it.h) * HD + ch * 32;
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(dst + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
-                    } else {
+                    {
                         const int64_t* sst = which == 0 ? a.dv_stride : a.dk_stride;
                         uint16_t* base = static_cast<uint16_t*>(which == 0 ? a.dv : a.dk);
                         uint16_t* dst = base + (thd ? prow * sst[1] : it.bi * sst[0] + kj * sst[1]) +
-                                        it.gk * sst[2] + ch * 32;
+                                        it.gk * sst[2] + ch * 16;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8)
+                        for (int e = 0; e < 16; e += 8)
                             *reinterpret_cast<uint4*>(dst + e) =
                                 make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
                                            pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
@@ -539,6 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         }
     } else {
         // ------------------------------------------------------------ dQ
+        // Visitors of a q-tile are the contiguous kv-tiles [first, first + n).
+        //  - n == 1: the lone visitor converts its dQ rows and stores them.
+        //  - deterministic mode, or n == 2: the tile is passed along the relay
+        //    (turn = t - first; wait until the counter equals the turn): the
+        //    first stores fp32 rows into the accumulator, middle turns add,
+        //    the last adds the accumulator to its registers, converts and
+        //    stores dQ. Sums run in kv-tile order: bitwise repeatable.
+        //  - otherwise (n >= 3): unordered vector atomics into the accumulator,
+        //    which the preprocess zeroed for these tiles; the dQ convert
+        //    kernel converts them.
         const int r = tid - kWarpDq0 * 32;  // q row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint32_t dq_it = 0;
@@ -546,25 +607,35 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode(a, item);
             if (!it.has_work) continue;
-            for (int64_t j = it.q_lo; j < it.q_hi; ++j) {
-                if (!(ok = wait_group(kBarDq, kDqFull, dq_it & 1))) break;
+            for (int64_t k = 0; k < it.steps; ++k) {
+                const int64_t j = it.qtile(k), hh = it.head(k);
+                if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
+                if (r == 0) SWA_TRACE(9, dq_it);
                 ++dq_it;
                 tc_fence_after();
-                const int64_t q0 = j * kTileQ;
-                const int64_t qi = q0 + r;
+                const int64_t qi = j * kTileQ + r;
                 const bool row_ok = qi < it.s.len_q;
-                float* dst = a.dq_acc + ((it.s.q_row0 + qi) * g.h_q + it.h) * HD;
-                int32_t* sem = nullptr;
-                int turn = 0;
-                bool turn_ok = true;
-                if (a.deterministic) {
-                    const int64_t first = g.window_left >= 0
-                        ? imax(floor_div(q0 + it.s.diag - g.window_left, kTileKV), 0) : 0;
-                    turn = static_cast<int>(it.t - first);
-                    sem = a.sems + (it.bi * g.h_q + it.h) * a.n_q_tiles + j;
+                const int64_t prow = it.s.q_row0 + qi;
+                int64_t first, nvis;
+                q_tile_visitors(g, it.s, j, first, nvis);
+                const int turn = static_cast<int>(it.t - first);
+                const bool single = nvis <= 1;
+                int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
+                float* acc = a.dq_acc + (prow * g.h_q + hh) * HD;
+                uint16_t* dqp = static_cast<uint16_t*>(a.dq) +
+                                (thd ? prow * a.dq_stride[1] : it.bi * a.dq_stride[0] + qi * a.dq_stride[1]) +
+                                hh * a.dq_stride[2];
+                // two visitors, or deterministic mode: hand the tile along in turn order
+                const bool relay = a.deterministic || nvis == 2;
+                const bool accumulate = !single && !relay;
+                const bool conv_now = single || (relay && turn == nvis - 1);
+                // Waits for this visit's turn (relay) or for the first visitor's store.
+                auto wait_turn = [&]() -> bool {
+                    if (!relay || turn == 0) return true;
                     if (r == 0) {
                         const uint64_t t0 = globaltimer_ns();
-                        while (ld_acquire_gpu(sem) != turn) {
+                        for (;;) {
+                            if (ld_acquire_gpu(sem) == turn) break;
                             if (*abort_flag || globaltimer_ns() - t0 > tmo) {
                                 set_status(a.status, kStatusTimeout);
                                 *abort_flag = 1;
@@ -573,29 +644,75 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         }
                     }
                     named_bar_sync(kBarDq, 128);
-                    turn_ok = *abort_flag == 0;
-                }
-#pragma unroll 1
-                for (int ch = 0; ch < HD / 32; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + C::kColDQ + lane_off + ch * 32, v);
-                    tmem_ld_wait();
-                    if (row_ok && turn_ok) {
+                    return *abort_flag == 0;
+                };
+                // Writes 32 dQ values of this row: converted (plus the partial sum
+                // of the earlier visitors unless alone), stored as the first
+                // partial, or added to it.
+                auto emit = [&](int col, float (&f)[32]) {
+                    if (conv_now) {
+                        if (!single) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                const float4 o = ld_cg_f4(acc + col + e);
+                                f[e] += o.x; f[e + 1] += o.y; f[e + 2] += o.z; f[e + 3] += o.w;
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            *reinterpret_cast<uint4*>(dqp + col + e) =
+                                make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
+                                           pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
+                    } else if (turn == 0 && !accumulate) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
-                            red_add_v4(dst + ch * 32 + e, __uint_as_float(v[e]) * a.scale,
-                                       __uint_as_float(v[e + 1]) * a.scale,
-                                       __uint_as_float(v[e + 2]) * a.scale,
-                                       __uint_as_float(v[e + 3]) * a.scale);
+                            *reinterpret_cast<float4*>(acc + col + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) red_add_v4(acc + col + e, f[e], f[e + 1], f[e + 2], f[e + 3]);
                     }
+                };
+                bool turn_ok = true;
+                if constexpr (HD == 64) {
+                    // the whole row fits in registers: free TMEM before any wait
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem + C::kColDQ + lane_off, v0);
+                    tmem_ld32(tmem + C::kColDQ + lane_off + 32, v1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(kDqEmpty));
+                    if (r == 0) SWA_TRACE(10, dq_it - 1);
+                    float f0[32], f1[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        f0[e] = __uint_as_float(v0[e]) * a.scale;
+                        f1[e] = __uint_as_float(v1[e]) * a.scale;
+                    }
+                    turn_ok = wait_turn();
+                    if (row_ok && turn_ok) {
+                        emit(0, f0);
+                        emit(32, f1);
+                    }
+                } else {
+                    turn_ok = wait_turn();
+#pragma unroll 1
+                    for (int ch = 0; ch < HD / 32; ++ch) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + C::kColDQ + lane_off + ch * 32, v);
+                        tmem_ld_wait();
+                        float f[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * a.scale;
+                        if (row_ok && turn_ok) emit(ch * 32, f);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(kDqEmpty));
                 }
-                tc_fence_before();
-                mbar_arrive(bar(kDqEmpty));
-                if (a.deterministic) {
-                    __threadfence();
-                    named_bar_sync(kBarDq, 128);
-                    if (r == 0) st_release_gpu(sem, turn + 1);
-                }
+                if (r == 0) SWA_TRACE(11, dq_it - 1);
+                if (!relay) continue;
+                // publish: the group's writes are ordered before one release
+                named_bar_sync(kBarDq, 128);
+                if (r == 0 && turn + 1 < nvis) st_release_gpu(sem, turn + 1);
             }
         }
     }
@@ -615,7 +732,7 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     const uint32_t bytes = Cfg<HD>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    const int64_t items = a.g.b * a.g.h_q * a.n_kv_tiles;
+    const int64_t items = a.g.b * a.g.h_kv * a.n_kv_tiles;
     if (items == 0) return cudaSuccess;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

@@ -23,8 +23,6 @@ struct WsLayout {
     size_t delta;       // fp32, indexed like LSE
     size_t sems;        // int32 [b][h_q][n_q_tiles]
     size_t dsink_part;  // fp32 [h_q][n_row_blocks]
-    size_t dk_ws;       // fp32 [rows_kv][h_q][d]  (GQA only)
-    size_t dv_ws;       // fp32 [rows_kv][h_q][d]  (GQA only)
     size_t total;
     int64_t n_sems;
     int64_t n_row_blocks;
@@ -51,7 +49,8 @@ struct PreArgs {
     const float* lse;
     const float* sink;
     int64_t o_stride[3], do_stride[3];
-    float* dq_acc;
+    float* dq_acc;       // zeroed here on q-tiles that take unordered atomics
+    int32_t deterministic;
     float* delta;
     int32_t* status;     // status + ticket (2 ints)
     int32_t* sems;
@@ -68,9 +67,10 @@ struct MainArgs {
     const void *q, *k, *v, *dout;
     const float* lse;
     const float* delta;
-    float* dq_acc;
-    void *dk, *dv;
-    float *dk_ws, *dv_ws;     // non-null: GQA partial output
+    float* dq_acc;            // fp32 partial sums of q-tiles with several visitors
+    void* dq;                 // dQ output (I/O dtype), written by each q-tile's last visitor
+    int64_t dq_stride[3];
+    void *dk, *dv;            // dK, dV (I/O dtype), summed over each kv-head's group
     int32_t* status;
     int32_t* sems;
     int64_t q_stride[3], k_stride[3], v_stride[3], do_stride[3], dk_stride[3], dv_stride[3];
@@ -84,7 +84,8 @@ struct MainArgs {
 
 struct CvtArgs {
     Geometry g;
-    const float* dq_acc;
+    const float* dq_acc;  // converted here on q-tiles that took unordered atomics
+    int32_t deterministic;
     void* dq;
     int64_t dq_stride[3];
     const float* dsink_part;
@@ -92,17 +93,9 @@ struct CvtArgs {
     float* dsink;
 };
 
-struct ReduceArgs {
-    Geometry g;
-    const float *dk_ws, *dv_ws;
-    void *dk, *dv;
-    int64_t dk_stride[3], dv_stride[3];
-};
-
 // Launchers (defined next to their kernels). Return the launch error.
 cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s);
-cudaError_t launch_gqa_reduce(const ReduceArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_main(const MainArgs& a, int dtype, cudaStream_t s);
 
 }  // namespace swa

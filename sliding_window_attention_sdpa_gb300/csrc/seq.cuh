@@ -75,4 +75,62 @@ __device__ __forceinline__ void set_status(int32_t* status, int code)
     atomicCAS(status, 0, code);
 }
 
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ int64_t fdiv(int64_t a, int64_t b)
+{
+    int64_t q = a / b;
+    if ((a % b != 0) && ((a < 0) != (b < 0))) --q;
+    return q;
+}
+
+// q-tile range [lo, hi) swept by kv-tile t of a sequence: lo is the first
+// q-tile holding a row that reaches the tile's first key (right bound), hi the
+// clamp ceil((kv_end + W - diag) / tile_q) with kv_end the tile's last key + 1
+// (cuDNN-frontend PR #866, "Change").
+__device__ __forceinline__ void q_tile_range(const Geometry& g, const SeqInfo& s, int64_t t,
+                                             int64_t& lo, int64_t& hi)
+{
+    const int64_t kv_base = t * kTileKV;
+    const int64_t n_q = (s.len_q + kTileQ - 1) / kTileQ;
+    lo = 0;
+    hi = n_q;
+    if (kv_base >= s.len_kv || n_q == 0) {
+        hi = 0;
+        return;
+    }
+    const int64_t kv_end = imin64(kv_base + kTileKV, s.len_kv);
+    if (g.right >= 0) {
+        const int64_t first = kv_base - g.right - s.diag;
+        lo = first > 0 ? first / kTileQ : 0;
+    }
+    if (g.window_left >= 0) {
+        const int64_t c = fdiv(kv_end + g.window_left - s.diag + kTileQ - 1, kTileQ);
+        if (c < hi) hi = c;
+    }
+    if (hi < lo) hi = lo;
+}
+
+// The kv-tiles that sweep q-tile j: the contiguous run [first, first + count)
+// (both bounds of q_tile_range are non-decreasing in t). `first` is the relay's
+// kv_first = max((q_row0 + diag - W) // tile_kv, 0) (PR #866, "Change"), or 0
+// without a left window.
+__device__ __forceinline__ void q_tile_visitors(const Geometry& g, const SeqInfo& s, int64_t j,
+                                                int64_t& first, int64_t& count)
+{
+    const int64_t n_kv = (s.len_kv + kTileKV - 1) / kTileKV;
+    first = 0;
+    count = 0;
+    if (n_kv == 0 || j * kTileQ >= s.len_q) return;
+    if (g.window_left >= 0) first = imax64(fdiv(j * kTileQ + s.diag - g.window_left, kTileKV), 0);
+    int64_t last = n_kv - 1;
+    if (g.right >= 0) last = imin64(last, fdiv((j + 1) * kTileQ + g.right + s.diag - 1, kTileKV));
+    if (last < first) return;
+    int64_t lo, hi;
+    q_tile_range(g, s, first, lo, hi);
+    if (!(lo <= j && j < hi)) return;
+    count = last - first + 1;
+}
+
 }  // namespace swa

@@ -46,6 +46,13 @@ SMALL = [
          thd_lens=[390, 64, 1000], slot_align=8, seed=14),
     Case("br_q_longer_than_kv_lens", 2, 2, 2, 400, 400, 64, "br", 40, lens_q=[400, 300],
          lens_kv=[150, 400], seed=15),
+    # window-only with more queries than keys: rows past Lkv + W reach no key
+    Case("none_w50_q600_kv300", 1, 2, 2, 600, 300, 64, "none", 50, seed=16),
+    # many visitors per q-tile (unordered atomics path) with GQA and a sink
+    Case("tl_w700_gqa4x2_sink_s900", 1, 4, 2, 900, 900, 64, "tl", 700, sink=True, seed=17),
+    Case("tl_w700_gqa4x2_sink_s900_det", 1, 4, 2, 900, 900, 64, "tl", 700, sink=True, det=True,
+         seed=17),
+    Case("none_w300_d128_f16", 1, 2, 2, 700, 700, 128, "none", 300, dtype="f16", seed=18),
 ]
 
 
@@ -124,6 +131,8 @@ FULL = [
           seed=1003, gen_device="cuda"), [(0, 0), (7, 3)]),
     (Case("winonly_b4_h16_d64_s4096_w512", 4, 16, 16, 4096, 4096, 64, "none", 512, seed=1004,
           gen_device="cuda"), [(2, 9)]),
+    (Case("gqa_b24_h28x4_d128_s128_br_w8000_f16", 24, 28, 4, 128, 128, 128, "br", 8000,
+          dtype="f16", seed=1006, gen_device="cuda"), [(bi, g) for bi in range(24) for g in range(4)]),
 ]
 
 
