@@ -177,6 +177,33 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one main-kernel
+# launch from an ncu capture (profiles/sdpa_bwd_main_kernel_*.md), valid only
+# for the kernel source it was taken on (sha256 of the main kernel's sources,
+# first 16 hex digits); any other source reports null.
+MAIN_TRAFFIC = {
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "1632ef6bc26c1423", "bytes": 250243840},
+}
+KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
+
+
+def main_kernel_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sliding_window_attention_sdpa_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(name: str):
+    t = MAIN_TRAFFIC.get(name)
+    if t is None or t["kernel"] != main_kernel_digest():
+        return None
+    return t["bytes"]
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -400,7 +427,7 @@ def main():
         "deterministic": bool(args.deterministic),
         "device_status": int(status),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
-                     "frac": achieved / peak_gbs, "traffic": None,
+                     "frac": achieved / peak_gbs, "traffic": measured_traffic(args.workload),
                      "kernel": "sdpa_bwd_main_kernel", "peak_kind": peak_kind,
                      "algorithmic_bytes": prob.main_bytes},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_max,

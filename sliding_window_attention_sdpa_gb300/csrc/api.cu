@@ -120,14 +120,14 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     const int64_t rq = rows_q(p);
     const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
     w.n_sems = p->b * p->h_q * nqt;
-    w.n_row_blocks = p->b * ((p->s_q + swa::kPreRows - 1) / swa::kPreRows);
+    w.n_row_blocks = p->b * ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * (swa::kTileQ / swa::kPreRows);
     size_t off = 0;
     w.status = off;
     off = align256(off + 16);
     w.dq_acc = off;
     off = align256(off + static_cast<size_t>(rq) * p->h_q * p->d * 4);
-    w.delta = off;
-    off = align256(off + static_cast<size_t>(rq) * p->h_q * 4);
+    w.stats = off;
+    off = align256(off + static_cast<size_t>(p->b) * p->h_q * nqt * swa::kTileQ * 8);
     w.sems = off;
     off = align256(off + static_cast<size_t>(w.n_sems) * 4);
     w.dsink_part = off;
@@ -283,7 +283,8 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
     copy3(a.do_stride, p->do_stride);
     a.dq_acc = at<float>(ws, w.dq_acc);
     a.deterministic = p->deterministic;
-    a.delta = at<float>(ws, w.delta);
+    a.stats = at<float2>(ws, w.stats);
+    a.stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
     a.status = at<int32_t>(ws, w.status);
     a.sems = at<int32_t>(ws, w.sems);
     a.n_sems = w.n_sems;
@@ -311,8 +312,8 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     a.k = p->k;
     a.v = p->v;
     a.dout = p->dout;
-    a.lse = p->lse;
-    a.delta = at<float>(ws, w.delta);
+    a.stats = at<float2>(ws, w.stats);
+    a.stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
     a.dq_acc = at<float>(ws, w.dq_acc);
     a.dq = p->dq;
     copy3(a.dq_stride, p->dq_stride);

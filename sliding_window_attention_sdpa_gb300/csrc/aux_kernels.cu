@@ -53,7 +53,8 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 }
 
 // ---------------------------------------------------------------- preprocess
-// grid (ceil(s_q / 64), h_q, b): 64 rows of one sequence's slot for one q-head.
+// grid (ceil(s_q / 128) * 2, h_q, b): 64 rows of one sequence's slot for one
+// q-head, covering every row of every q-tile (rows past the length included).
 // Each row of HD features is read by HD/8 consecutive threads (16 B each).
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
@@ -80,10 +81,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
     }
     const SeqInfo s = seq_info(g, bi);
     const int64_t blk = bi * gridDim.x + blockIdx.x;  // dSink partial slot
-    if (i0 >= s.slot_q) {
-        if (with_sink && tid == 0) a.dsink_part[h * a.n_row_blocks + blk] = 0.f;
-        return;
-    }
     const float sink = with_sink ? a.sink[h] : 0.f;
     // q-tiles with three or more visitors take unordered atomics (unless
     // deterministic): their accumulator rows start at zero
@@ -101,7 +98,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
 #pragma unroll 2
     for (int r = tid / TPR; r < kPreRows; r += RPP) {
         const int64_t i = i0 + r;
-        const bool in_slot = i < s.slot_q;
         const bool valid = i < s.len_q;
         float part = 0.f;
         if (valid) {
@@ -122,13 +118,20 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (in_slot && c == 0) {
-            const int64_t so = thd ? h * g.rows_q + s.q_row0 + i : (bi * g.h_q + h) * g.s_q + i;
-            a.delta[so] = valid ? part : 0.f;
-            if (with_sink && valid) {
+        if (c == 0) {
+            // per-row statistics for the main kernel, one slot for every row of
+            // every q-tile: (LSE * log2(e), D); rows past the length or that
+            // attend nothing get (+inf, 0) so that P = 0 there
+            float l2 = INFINITY;
+            if (valid) {
+                const int64_t so = thd ? h * g.rows_q + s.q_row0 + i : (bi * g.h_q + h) * g.s_q + i;
                 const float lse = a.lse[so];
-                if (lse != -INFINITY) dsink_acc -= expf(sink - lse) * part;
+                if (lse != -INFINITY) {
+                    l2 = lse * 1.4426950408889634f;
+                    if (with_sink) dsink_acc -= expf(sink - lse) * part;
+                }
             }
+            a.stats[(bi * g.h_q + h) * a.stats_row + i] = make_float2(l2, valid ? part : 0.f);
         }
     }
 
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
 
 cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
 {
-    const int64_t nx = (a.g.s_q + kPreRows - 1) / kPreRows;
+    const int64_t nx = a.stats_row / kPreRows;  // every row of every q-tile
     if (nx == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(nx), static_cast<unsigned>(a.g.h_q), static_cast<unsigned>(a.g.b));
     SWA_DISPATCH(preprocess_kernel, a, grid, s);

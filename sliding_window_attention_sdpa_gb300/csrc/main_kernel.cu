@@ -20,7 +20,8 @@
 //   warp 0      TMA producer: K, V per item; Q, dO per q-tile into a ring of
 //               kStages stages (128-byte swizzle, zero fill past the tensor)
 //   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2-3   LSE / D loader: the q-tile's 128 LSE (log2 domain) and D values
+//   warps 2-3   idle (the q-tile's per-row (LSE log2, D) pairs arrive with the
+//               producer's Q/dO loads as one 1 KB bulk copy)
 //   warps 4-11  softmax: two warps per TMEM sub-partition, each thread one kv
 //               row (TMEM lane) and one 64-column half of the q-tile; recomputes
 //               P = exp2(S*scale*log2e - LSE*log2e) and dS = P (dP - D) with the
@@ -54,8 +55,7 @@ constexpr uint32_t kBlock16K = 128 * 128;  // one 64-column block of a 128-row t
 constexpr float kLog2e = 1.4426950408889634f;
 
 // warp roles
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLse0 = 2, kWarpSoft0 = 4, kWarpDq0 = 12;
-constexpr int kLseThreads = 64;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSoft0 = 4, kWarpDq0 = 12;
 constexpr int kSoftThreads = 256;
 constexpr int kBarDq = 1, kBarSoft = 2;  // named barriers of the two 128-thread groups
 
@@ -72,9 +72,8 @@ struct Cfg {
     static constexpr bool kPInTmem = HD == 64;                  // P^T kept in TMEM
     static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q] (d = 128)
     static constexpr uint32_t kDS = kP + (kPInTmem ? 0 : 32768); // dS^T [128 kv x 128 q]
-    static constexpr uint32_t kLse = kDS + 32768;               // kStages x 128 fp32
-    static constexpr uint32_t kDelta = kLse + kStages * 512;    // kStages x 128 fp32
-    static constexpr uint32_t kBars = kDelta + kStages * 512;   // mbarriers
+    static constexpr uint32_t kStat = kDS + 32768;              // kStages x 128 float2
+    static constexpr uint32_t kBars = kStat + kStages * 1024;   // mbarriers
     static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags
     static constexpr uint32_t kBytes = kMisc + 64;
     static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -263,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         mbar_init(bar(kAccFull), 1);
         mbar_init(bar(kAccEmpty), kSoftThreads);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar(kQFull0 + s), 1 + kLseThreads);
+            mbar_init(bar(kQFull0 + s), 1);
             mbar_init(bar(kQEmpty0 + s), 1);
         }
         fence_mbar_init();
@@ -317,11 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
                     SWA_TRACE(12, q_it);
                     const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
-                    mbar_arrive_expect_tx(bar(kQFull0 + st), 2 * C::kTile);
+                    mbar_arrive_expect_tx(bar(kQFull0 + st), 2 * C::kTile + 1024);
                     tma_tile<HD>(sbase + C::kQ + st * C::kTile, &a.tm_q, bar(kQFull0 + st), thd,
                                  (int)hh, qrow, (int)it.bi);
                     tma_tile<HD>(sbase + C::kDO + st * C::kTile, &a.tm_do, bar(kQFull0 + st), thd,
                                  (int)hh, qrow, (int)it.bi);
+                    bulk_load(sbase + C::kStat + st * 1024,
+                              a.stats + (static_cast<int64_t>(it.bi) * g.h_q + hh) * a.stats_row +
+                                  static_cast<int64_t>(j) * kTileQ,
+                              1024, bar(kQFull0 + st));
                     SWA_TRACE(13, q_it);
                 }
                 if (!ok) break;
@@ -422,36 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             ++acc_it;
         }
     } else if (warp < kWarpSoft0) {
-        // ------------------------------------------------------------ LSE / D loader
-        const int lt = tid - kWarpLse0 * 32;  // 0..63, two rows each
-        uint32_t q_it = 0;
-        bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode(a, item);
-            if (!it.has_work) continue;
-            for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
-                const int64_t j = it.qtile(k), hh = it.head(k);
-                const int st = q_it % C::kStages;
-                if (!(ok = wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1))) break;
-                float* sl = reinterpret_cast<float*>(sm + C::kLse + st * 512);
-                float* sd = reinterpret_cast<float*>(sm + C::kDelta + st * 512);
-#pragma unroll
-                for (int r = lt; r < 128; r += kLseThreads) {
-                    const int64_t qi = j * kTileQ + r;
-                    float lse = INFINITY, dlt = 0.f;
-                    if (qi < it.s.len_q) {
-                        const int64_t so = stat_offset(g, it.s.q_row0 + qi, hh);
-                        lse = a.lse[so];
-                        dlt = a.delta[so];
-                        if (lse == -INFINITY) lse = INFINITY;  // row attends nothing: P = 0
-                    }
-                    sl[r] = lse * kLog2e;
-                    sd[r] = dlt;
-                }
-                mbar_arrive(bar(kQFull0 + st));
-                if (lt == 0) SWA_TRACE(14, q_it);
-            }
-        }
+        // warps 2-3: no role
     } else if (warp < kWarpDq0) {
         // ------------------------------------------------------------ softmax + dK/dV epilogue
         const int r = (warp & 3) * 32 + lane;        // kv row within the tile = TMEM lane
@@ -478,8 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         SWA_TRACE(warp == kWarpSoft0 ? 5 : 7, q_it);
                     ++s_it;
                     tc_fence_after();
-                    const float* sl = reinterpret_cast<const float*>(sm + C::kLse + st * 512);
-                    const float* sd = reinterpret_cast<const float*>(sm + C::kDelta + st * 512);
+                    const float2* stv = reinterpret_cast<const float2*>(sm + C::kStat + st * 1024);
                     const int64_t q0 = j * kTileQ;
                     const int c_lo = static_cast<int>(imax(i_lo - q0, 0));
                     const int c_hi = static_cast<int>(imin(i_hi - q0, 127));
@@ -501,11 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             if (full) {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
-                                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -sl[c0 + e]));
-                                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -sl[c0 + e + 1]));
+                                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -stv[c0 + e].x));
+                                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -stv[c0 + e + 1].x));
                                     pk[e >> 1] = pack2<BF16>(p0, p1);
-                                    dk[e >> 1] = pack2<BF16>(p0 * (__uint_as_float(dpv[e]) - sd[c0 + e]),
-                                                             p1 * (__uint_as_float(dpv[e + 1]) - sd[c0 + e + 1]));
+                                    dk[e >> 1] = pack2<BF16>(p0 * (__uint_as_float(dpv[e]) - stv[c0 + e].y),
+                                                             p1 * (__uint_as_float(dpv[e + 1]) - stv[c0 + e + 1].y));
                                 }
                             } else {
 #pragma unroll
@@ -516,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                         const int c = c0 + e + u;
                                         const bool att = c >= c_lo && c <= c_hi;
                                         const float p = att ? ex2_approx(fmaf(__uint_as_float(sv[e + u]),
-                                                                             a.scale_log2, -sl[c]))
+                                                                             a.scale_log2, -stv[c].x))
                                                             : 0.f;
                                         p2[u] = p;
-                                        d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - sd[c]) : 0.f;
+                                        d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - stv[c].y) : 0.f;
                                     }
                                     pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
                                     dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);

@@ -20,7 +20,7 @@ constexpr int kStatusBadLengths = 5;
 struct WsLayout {
     size_t status;      // int32 status, int32 ticket counter
     size_t dq_acc;      // fp32 [rows_q][h_q][d]
-    size_t delta;       // fp32, indexed like LSE
+    size_t stats;       // float2 (LSE * log2(e), D) per row, [b][h_q][n_q_tiles * 128]
     size_t sems;        // int32 [b][h_q][n_q_tiles]
     size_t dsink_part;  // fp32 [h_q][n_row_blocks]
     size_t total;
@@ -51,7 +51,8 @@ struct PreArgs {
     int64_t o_stride[3], do_stride[3];
     float* dq_acc;       // zeroed here on q-tiles that take unordered atomics
     int32_t deterministic;
-    float* delta;
+    float2* stats;       // (LSE * log2(e) or +inf where nothing is attended, D)
+    int64_t stats_row;   // entries per (sequence, q-head): n_q_tiles * 128
     int32_t* status;     // status + ticket (2 ints)
     int32_t* sems;
     int64_t n_sems;
@@ -65,8 +66,8 @@ struct MainArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
     Geometry g;
     const void *q, *k, *v, *dout;
-    const float* lse;
-    const float* delta;
+    const float2* stats;      // per-row (LSE * log2(e), D), tile-aligned (see PreArgs)
+    int64_t stats_row;
     float* dq_acc;            // fp32 partial sums of q-tiles with several visitors
     void* dq;                 // dQ output (I/O dtype), written by each q-tile's last visitor
     int64_t dq_stride[3];
