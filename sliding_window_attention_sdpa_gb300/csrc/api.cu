@@ -222,24 +222,24 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// TMA descriptor of one head-strided 16-bit tensor: 64 x 1 x 128 (x 1) boxes,
-// 128-byte swizzle, zero fill outside the tensor. Sizes of 1 get a harmless
-// non-zero stride.
-sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int dtype, bool thd,
-                       int64_t d, int64_t h, int64_t rows, int64_t b, const int64_t* st)
+// TMA descriptor of one head-strided tensor (strides in elements): boxes of
+// `box_d` x 1 x 128 (x 1) elements with the 128-byte swizzle (box_d elements
+// span 128 bytes), zero fill outside the tensor. BSHD maps are 4-D (d, h, s, b),
+// THD maps 3-D (d, h, t). Sizes of 1 get a harmless non-zero stride.
+sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, CUtensorMapDataType dt,
+                       int64_t esize, uint32_t box_d, bool thd, int64_t d, int64_t h, int64_t rows,
+                       int64_t b, const int64_t* st)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-    const CUtensorMapDataType dt =
-        dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const cuuint64_t row_bytes = static_cast<cuuint64_t>(d) * 2;
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(d * esize);
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
                           static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(b)};
-    cuuint64_t hs = h > 1 ? static_cast<cuuint64_t>(st[2]) * 2 : row_bytes;
-    cuuint64_t ss = rows > 1 ? static_cast<cuuint64_t>(st[1]) * 2 : hs * h;
-    cuuint64_t bs = b > 1 ? static_cast<cuuint64_t>(st[0]) * 2 : ss * (rows > 0 ? rows : 1);
+    cuuint64_t hs = h > 1 ? static_cast<cuuint64_t>(st[2] * esize) : row_bytes;
+    cuuint64_t ss = rows > 1 ? static_cast<cuuint64_t>(st[1] * esize) : hs * h;
+    cuuint64_t bs = b > 1 ? static_cast<cuuint64_t>(st[0] * esize) : ss * (rows > 0 ? rows : 1);
     cuuint64_t strides[3] = {hs, ss, bs};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {box_d, 1, 128, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const cuuint32_t rank = thd ? 3 : 4;
     CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
@@ -250,6 +250,15 @@ sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int d
                     "%s: TMA descriptor rejected (error %d) for strides (%lld, %lld, %lld)", name,
                     (int)r, (long long)st[0], (long long)st[1], (long long)st[2]);
     return SDPA_OK;
+}
+
+// Descriptor of a 16-bit I/O tensor (64-element boxes).
+sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int dtype, bool thd,
+                       int64_t d, int64_t h, int64_t rows, int64_t b, const int64_t* st)
+{
+    const CUtensorMapDataType dt =
+        dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return make_map(m, name, base, dt, 2, 64, thd, d, h, rows, b, st);
 }
 
 template <typename T>
@@ -348,8 +357,22 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     if ((st = make_map(&a.tm_q, "q", qptr, p->dtype, thd, p->d, hq_map, rq_map, p->b, qst)) != SDPA_OK ||
         (st = make_map(&a.tm_do, "dout", doptr, p->dtype, thd, p->d, hq_map, rq_map, p->b, dost)) != SDPA_OK ||
         (st = make_map(&a.tm_k, "k", p->k, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->k_stride)) != SDPA_OK ||
-        (st = make_map(&a.tm_v, "v", p->v, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->v_stride)) != SDPA_OK)
+        (st = make_map(&a.tm_v, "v", p->v, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->v_stride)) != SDPA_OK ||
+        (st = make_map(&a.tm_dk, "dk", p->dk, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->dk_stride)) != SDPA_OK ||
+        (st = make_map(&a.tm_dv, "dv", p->dv, p->dtype, thd, p->d, p->h_kv, rk_map, p->b, p->dv_stride)) != SDPA_OK)
         return st;
+    // dQ and its fp32 accumulator ([rows][h_q][d], packed). With no q rows they
+    // are placeholders over K, never used.
+    const int64_t acc_st[3] = {p->s_q * p->h_q * p->d, p->h_q * p->d, p->d};
+    if (rq > 0) {
+        if ((st = make_map(&a.tm_dq, "dq", p->dq, p->dtype, thd, p->d, p->h_q, rq, p->b, p->dq_stride)) != SDPA_OK ||
+            (st = make_map(&a.tm_acc, "dq accumulator", a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, thd,
+                           p->d, p->h_q, rq, p->b, acc_st)) != SDPA_OK)
+            return st;
+    } else {
+        a.tm_dq = a.tm_k;
+        a.tm_acc = a.tm_k;
+    }
     return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
 }
 
@@ -393,6 +416,8 @@ sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
     if (host[0] == SDPA_ERR_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a relay or MMA wait ran out on the device");
     if (host[0] == SDPA_ERR_BAD_LENGTHS)
         return fail(SDPA_ERR_BAD_LENGTHS, "a sequence length exceeds its slot (or s_q/s_kv)");
+    if (host[0] == SDPA_ERR_UNSUPPORTED)
+        return fail(SDPA_ERR_UNSUPPORTED, "the device gave the main kernel shared memory not 1024-byte aligned");
     if (host[0] != 0) return fail(SDPA_ERR_CUDA, "unknown device status %d", host[0]);
     return SDPA_OK;
 }

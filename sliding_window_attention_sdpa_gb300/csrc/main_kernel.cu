@@ -18,18 +18,23 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: K, V per item; Q, dO per q-tile into a ring of
-//               kStages stages (128-byte swizzle, zero fill past the tensor)
-//   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2-3   idle (the q-tile's per-row (LSE log2, D) pairs arrive with the
-//               producer's Q/dO loads as one 1 KB bulk copy)
+//               kStages stages (128-byte swizzle, zero fill past the tensor),
+//               each with the q-tile's per-row (LSE log2, D) pairs (1 KB bulk copy)
+//   warp 1      MMA issuer (one thread) and TMEM owner. At d = 64 it issues the
+//               next q-tile's S^T/dP^T ahead of this q-tile's dV/dK/dQ, so the
+//               softmax of one q-tile overlaps the gradient contractions of the
+//               previous one (dS^T double-buffered)
+//   warps 2-3   idle
 //   warps 4-11  softmax: two warps per TMEM sub-partition, each thread one kv
 //               row (TMEM lane) and one 64-column half of the q-tile; recomputes
 //               P = exp2(S*scale*log2e - LSE*log2e) and dS = P (dP - D) with the
-//               mask, skipping 32-column chunks the window masks for the whole
+//               mask, skipping 16-column chunks the window masks for the whole
 //               warp; writes P^T / dS^T as swizzled 16-bit tiles; at the end of
-//               an item one half stores dV, the other dK (or fp32 GQA partials)
-//   warps 12-15 dQ: one thread per q row reads dQ from TMEM and adds it to the
-//               fp32 accumulator (vector atomics, or the ordered relay)
+//               an item one half writes dV, the other dK, through a staged tile
+//   warps 12-15 dQ: one thread per q row reads dQ from TMEM into a staged fp32
+//               tile, from which the group writes whole rows: converted, stored
+//               as the first partial sum, or added to the accumulator (vector
+//               atomics, or in order along the relay)
 // Hand-offs are mbarriers; every wait is bounded (status word on timeout).
 //
 // Shared-memory operand layout: rows of 64 16-bit elements (128 B), 8-row
@@ -63,6 +68,13 @@ template <int HD>
 struct Cfg {
     static constexpr int kStages = HD == 64 ? 2 : 1;    // Q/dO/LSE/D ring
     static constexpr int kKvStages = HD == 64 ? 2 : 1;  // K/V ring (per work item)
+    // d = 64: the next q-tile's S^T/dP^T contractions are issued ahead of this
+    // q-tile's gradient contractions, so that the softmax runs while the tensor
+    // core works; dS^T is double-buffered for it. Both rings must hold two
+    // entries, or the look-ahead would wait on a buffer it has yet to release.
+    static constexpr bool kAhead = HD == 64;
+    static constexpr int kDsBufs = kAhead ? 2 : 1;
+    static_assert(!kAhead || (kStages >= 2 && kKvStages >= 2), "look-ahead needs two ring entries");
     static constexpr uint32_t kTile = 128 * HD * 2;
     // shared memory offsets (from a 1024-aligned base)
     static constexpr uint32_t kK = 0;                           // kKvStages tiles
@@ -71,22 +83,32 @@ struct Cfg {
     static constexpr uint32_t kDO = kQ + kStages * kTile;       // kStages tiles
     static constexpr bool kPInTmem = HD == 64;                  // P^T kept in TMEM
     static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q] (d = 128)
-    static constexpr uint32_t kDS = kP + (kPInTmem ? 0 : 32768); // dS^T [128 kv x 128 q]
-    static constexpr uint32_t kStat = kDS + 32768;              // kStages x 128 float2
+    static constexpr uint32_t kDS = kP + (kPInTmem ? 0 : 32768); // kDsBufs x dS^T [128 kv x 128 q]
+    // dQ staging: 128 rows x 64 fp32 (two 16 KB blocks of 32 columns; the whole
+    // row at d = 64, half of it at d = 128), or the whole 16-bit dQ tile
+    static constexpr int kDqCols = 64;
+    static constexpr uint32_t kDqStage = kDS + kDsBufs * 32768;
+    static constexpr uint32_t kStat = kDqStage + 128 * kDqCols * 4;  // kStages x 128 float2
     static constexpr uint32_t kBars = kStat + kStages * 1024;   // mbarriers
     static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags
     static constexpr uint32_t kBytes = kMisc + 64;
-    static constexpr uint32_t kAlloc = kBytes + 1024;
+    static_assert(kBytes <= 232448, "shared memory above the 227 KB a CTA may opt into");
+    // The dK/dV epilogue stages two 128 x HD 16-bit tiles (2 x 16 KB at d = 64,
+    // 2 x 32 KB at d = 128) in a dS^T buffer (d = 64) or in the P^T + dS^T
+    // buffers (d = 128), all idle once the work item's contractions are done.
+    static_assert(kPInTmem ? 2 * 128 * HD * 2 <= 32768 : (kDS == kP + 32768 && 2 * 128 * HD * 2 <= 65536),
+                  "epilogue staging does not fit");
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
     static constexpr uint32_t kColDQ = HD == 64 ? 384 : 0;
     static constexpr uint32_t kColP = 448;                      // d = 64 only
     static constexpr bool kDqAliasesS = HD != 64;
+    static_assert(!(kAhead && kDqAliasesS), "look-ahead overwrites S^T while dQ would alias it");
 };
 
 // mbarrier indices
 enum Bar : int {
-    kSFull = 0, kPFull, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
+    kSFull = 0, kPFull, kPEmpty, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
     kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kNumBars
 };
 
@@ -127,6 +149,74 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Shared -> global tensor copies (bulk-group completion): a plain store, or an
+// element-wise add into global memory performed at L2 (fp32 maps only here).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_add_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+// One 128-row box of a [., h, d] tensor map at column c0 of head h: BSHD maps
+// are 4-D (d, h, s, b), THD maps 3-D (d, h, t); `row` is s (BSHD) or t (THD).
+__device__ __forceinline__ void tma_put(bool add, bool thd, const CUtensorMap* map, uint32_t src, int c0, int h,
+                                        int row, int b)
+{
+    if (add) {
+        if (thd) tma_add_3d(map, src, c0, h, row);
+        else tma_add_4d(map, src, c0, h, row, b);
+    } else {
+        if (thd) tma_store_3d(map, src, c0, h, row);
+        else tma_store_4d(map, src, c0, h, row, b);
+    }
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The copies committed so far have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// The copies committed so far are complete (their global writes performed).
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders the async proxy's global writes (completed bulk copies) before the
+// generic-proxy operations that follow, such as a release that publishes them.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Byte offset of 16-byte chunk c of row r in a staged tile of 128-byte rows:
+// blocks of 128 rows x 128 B (8 chunks), chunk c & 7 at position (c & 7) ^ (r % 8)
+// -- the layout a TMA 128-byte-swizzle box of 128 rows reads from shared memory.
+__device__ __forceinline__ uint32_t stg_off(int r, int c)
+{
+    return static_cast<uint32_t>((c >> 3) * kBlock16K + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
 // Loads rows [row, row + 128) of one head of a [., HD] tensor into a swizzled tile
 // (HD/64 boxes of 64 columns). BSHD maps are 4-D (d, h, s, b); THD maps 3-D (d, h, t).
 template <int HD>
@@ -164,7 +254,7 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool v)
 // role's hand-offs for the first kTraceCtas CTAs and kTraceTiles q-tiles, written
 // to the workspace at byte offset kTraceOffset (the caller sizes the workspace
 // for it). Off by default; it records and changes nothing else.
-constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceSlots = 16;
+constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceSlots = 20;
 constexpr size_t kTraceOffset = size_t(256) << 20;
 #ifdef SDPA_BWD_TRACE
 #define SWA_TRACE(slot, tile)                                                                    \
@@ -194,8 +284,14 @@ __device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
 {
     const Geometry& g = a.g;
     Item it;
-    it.t = item % a.n_kv_tiles;
-    it.gk = (item / a.n_kv_tiles) % g.h_kv;
+    // Head-fastest numbering: the CTAs running at one time cover all kv-heads
+    // of a few kv-tiles. In the [row][head][d] tensors one head is a narrow
+    // column of every row, so kv-tile-fastest numbering (all CTAs on one head)
+    // concentrates their loads and stores on a few memory partitions. The
+    // previous kv-tile of the same head (the dQ relay partner) is then item
+    // - h_kv, which runs in the same wave.
+    it.gk = item % g.h_kv;
+    it.t = (item / g.h_kv) % a.n_kv_tiles;
     it.bi = item / (a.n_kv_tiles * g.h_kv);
     it.group = g.h_q / g.h_kv;
     it.h0 = it.gk * it.group;
@@ -234,9 +330,15 @@ template <int HD, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a)
 {
     using C = Cfg<HD>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+    // The 128-byte-swizzled operand tiles need a 1024-byte aligned base; the
+    // dynamic shared memory is declared so, and checked rather than padded
+    // (the layout leaves no room for the padding at d = 64).
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) set_status(a.status, kStatusUnsupported);
+        return;
+    }
+    uint8_t* sm = smem_raw;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bars = sbase + C::kBars;
     auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
@@ -257,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         }
         mbar_init(bar(kSFull), 1);
         mbar_init(bar(kPFull), kSoftThreads);
+        mbar_init(bar(kPEmpty), 1);
         mbar_init(bar(kDqFull), 1);
         mbar_init(bar(kDqEmpty), 128);
         mbar_init(bar(kAccFull), 1);
@@ -338,6 +441,62 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const uint32_t tm_s = tmem + C::kColS, tm_dp = tmem + C::kColDP;
         const uint32_t tm_dv = tmem + C::kColDV, tm_dk = tmem + C::kColDK, tm_dq = tmem + C::kColDQ;
         uint32_t kv_it = 0, q_it = 0, p_it = 0, dq_it = 0, acc_it = 0;
+        // The q-tile step whose gradient contractions (dV, dK, dQ) are not yet
+        // issued: they need the softmax's P^T / dS^T of that step.
+        struct Pending {
+            bool valid, first, last;  // first / last step of its work item
+            int st, ks;               // Q/dO and K/V ring entries
+            uint32_t q_it;            // step index (selects the dS^T buffer)
+        };
+        Pending pend{false, false, false, 0, 0, 0u};
+        // dV += P^T dO, dK += dS^T Q, dQ = dS K for step `p` (softmax done).
+        auto issue_grads = [&](const Pending& p) -> bool {
+            if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
+            if (p.first && !wait_warp(kAccEmpty, (acc_it & 1) ^ 1)) return false;
+            ++dq_it;
+            const uint32_t sK = sbase + C::kK + p.ks * C::kTile;
+            const uint32_t sQ = sbase + C::kQ + p.st * C::kTile, sDO = sbase + C::kDO + p.st * C::kTile;
+            const uint32_t sDS = sbase + C::kDS + (p.q_it % C::kDsBufs) * 32768u;
+            if (lane == 0) {
+                SWA_TRACE(3, p.q_it);
+                tc_fence_after();
+                const uint32_t acc = p.first ? 0u : 1u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bdesc = sdesc_sw128(sDO + k * 2048, kBlock16K, 1024);
+                    if constexpr (C::kPInTmem) {
+                        umma_f16_ts(tm_dv, tmem + C::kColP + k * 8, bdesc, kIdPV, acc | (k > 0));
+                    } else {
+                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), bdesc, kIdPV,
+                                    acc | (k > 0));
+                    }
+                }
+                // P^T is free (and, with everything issued before, the dS^T
+                // buffer of the step before this one)
+                if constexpr (C::kAhead) umma_commit(bar(kPEmpty));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                    umma_f16_ss(tm_dk, sdesc_sw128(sDS + aoff, 16, 1024),
+                                sdesc_sw128(sQ + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    umma_f16_ss(tm_dq, sdesc_sw128(sDS + k * 2048, kBlock16K, 1024),
+                                sdesc_sw128(sK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
+                umma_commit(bar(kDqFull));
+                umma_commit(bar(kQEmpty0 + p.st));
+                SWA_TRACE(4, p.q_it);
+                if (p.last) {
+                    umma_commit(bar(kAccFull));
+                    umma_commit(bar(kKvEmpty0 + p.ks));
+                }
+            }
+            __syncwarp();
+            if (p.last) ++acc_it;
+            return true;
+        };
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode(a, item);
@@ -357,6 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (q0 + kTileQ > it.s.len_q) {
                     zero_tail<HD>(sm + C::kQ + st * C::kTile, it.s.len_q - q0, lane);
                     zero_tail<HD>(sm + C::kDO + st * C::kTile, it.s.len_q - q0, lane);
+                }
+                if (C::kAhead && pend.valid) {
+                    // P^T, dS^T of the pending step are written and the softmax
+                    // is done with S^T, dP^T
+                    if (!(ok = wait_warp(kPFull, p_it & 1))) break;
+                    if (lane == 0) SWA_TRACE(2, pend.q_it);
+                    ++p_it;
                 }
                 // S^T and dP^T overwrite TMEM that the previous dQ may alias
                 if (C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
@@ -379,50 +545,22 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     SWA_TRACE(1, q_it);
                 }
                 __syncwarp();
-                // P^T, dS^T ready in shared memory (softmax done with S^T, dP^T)
-                if (!(ok = wait_warp(kPFull, p_it & 1))) break;
-                if (lane == 0) SWA_TRACE(2, q_it);
-                ++p_it;
-                if (!C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
-                if (k == 0 && !(ok = wait_warp(kAccEmpty, (acc_it & 1) ^ 1))) break;
-                ++dq_it;
-                if (lane == 0) {
-                    SWA_TRACE(3, q_it);
-                    tc_fence_after();
-                    const uint32_t acc = k > 0 ? 1u : 0u;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint64_t bdesc = sdesc_sw128(sDO + k * 2048, kBlock16K, 1024);
-                        if constexpr (C::kPInTmem) {
-                            umma_f16_ts(tm_dv, tmem + C::kColP + k * 8, bdesc, kIdPV, acc | (k > 0));
-                        } else {
-                            const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                            umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), bdesc, kIdPV,
-                                        acc | (k > 0));
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dk, sdesc_sw128(sbase + C::kDS + aoff, 16, 1024),
-                                    sdesc_sw128(sQ + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        umma_f16_ss(tm_dq, sdesc_sw128(sbase + C::kDS + k * 2048, kBlock16K, 1024),
-                                    sdesc_sw128(sK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
-                    umma_commit(bar(kDqFull));
-                    umma_commit(bar(kQEmpty0 + st));
-                    SWA_TRACE(4, q_it);
-                    if (k + 1 == it.steps) {
-                        umma_commit(bar(kAccFull));
-                        umma_commit(bar(kKvEmpty0 + ks));
-                    }
+                const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it};
+                if constexpr (C::kAhead) {
+                    if (pend.valid && !(ok = issue_grads(pend))) break;
+                    pend = cur;
+                } else {
+                    if (!(ok = wait_warp(kPFull, p_it & 1))) break;
+                    if (lane == 0) SWA_TRACE(2, q_it);
+                    ++p_it;
+                    if (!(ok = issue_grads(cur))) break;
                 }
-                __syncwarp();
             }
-            if (!ok) break;
-            ++acc_it;
+        }
+        if (ok && pend.valid) {
+            ok = wait_warp(kPFull, p_it & 1);
+            ++p_it;
+            if (ok) issue_grads(pend);
         }
     } else if (warp < kWarpSoft0) {
         // warps 2-3: no role
@@ -432,6 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const int half = (warp - kWarpSoft0) >> 2;   // q columns [64 half, 64 half + 64)
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint32_t q_it = 0, s_it = 0, acc_it = 0;
+        // dS^T buffer that an epilogue's TMA store may still be reading (-1: none);
+        // the thread that issued it waits before the buffer is written again
+        int store_buf = -1;
+        auto release_buf = [&](int buf) {
+            if (store_buf == buf) {
+                if (r == 0) bulk_wait_read0();
+                store_buf = -1;
+            }
+        };
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
             const Item it = decode(a, item);
@@ -446,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
                     const int64_t j = it.qtile(k);
                     const int st = q_it % C::kStages;
+                    release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
                     if (!(ok = wait_group(kBarSoft, kSoftThreads, kQFull0 + st, (q_it / C::kStages) & 1))) break;
                     if (!(ok = wait_group(kBarSoft, kSoftThreads, kSFull, s_it & 1))) break;
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
@@ -456,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     const int64_t q0 = j * kTileQ;
                     const int c_lo = static_cast<int>(imax(i_lo - q0, 0));
                     const int c_hi = static_cast<int>(imin(i_hi - q0, 127));
+                    uint8_t* ds_buf = sm + C::kDS + (q_it % C::kDsBufs) * 32768u;
 #pragma unroll 1
                     for (int sc = 4 * half; sc < 4 * half + 4; ++sc) {
                         const int c0 = sc * 16;
@@ -499,6 +648,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                 }
                             }
                         }
+                        if constexpr (C::kAhead) {
+                            // Before the first write: the gradient contractions of
+                            // the previous step have read P^T, and (issued after all
+                            // those of the step before it) this dS^T buffer.
+                            if (sc == 4 * half && q_it > 0) {
+                                if (!(ok = wait_group(kBarSoft, kSoftThreads, kPEmpty, (q_it - 1) & 1))) break;
+                                tc_fence_after();
+                            }
+                        }
                         if constexpr (C::kPInTmem) {
                             tmem_st8(tmem + C::kColP + lane_off + sc * 8, pk);
                         }
@@ -508,10 +666,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             if constexpr (!C::kPInTmem)
                                 *reinterpret_cast<uint4*>(sm + C::kP + off) =
                                     make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
-                            *reinterpret_cast<uint4*>(sm + C::kDS + off) =
+                            *reinterpret_cast<uint4*>(ds_buf + off) =
                                 make_uint4(dk[4 * m], dk[4 * m + 1], dk[4 * m + 2], dk[4 * m + 3]);
                         }
                     }
+                    if (!ok) break;
                     if constexpr (C::kPInTmem) tmem_st_wait();
                     fence_proxy_async_smem();
                     tc_fence_before();
@@ -519,46 +678,80 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
                         SWA_TRACE(warp == kWarpSoft0 ? 6 : 8, q_it);
                 }
+                release_buf(static_cast<int>((q_it + C::kDsBufs - 1) % C::kDsBufs));   // the epilogue's staging
                 if (ok) ok = wait_group(kBarSoft, kSoftThreads, kAccFull, acc_it & 1);
+                if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                    SWA_TRACE(warp == kWarpSoft0 ? 16 : 17, q_it - 1);
                 ++acc_it;
                 if (ok) tc_fence_after();
             }
-            // epilogue: half 0 stores this kv row's dV, half 1 its dK (scaled)
+            // Epilogue: half 0 writes the tile's dV, half 1 its dK (scaled). Each
+            // thread converts its kv row from TMEM into a staged 16-bit tile
+            // (128-byte-swizzle layout), which one thread stores with TMA; a tile
+            // ending past its sequence's slot (THD) is stored row-wise instead.
+            // Rows past the sequence's length are zero; rows past its slot (or
+            // past s_kv, where the BSHD maps end) are not written.
             if (!it.in_slot) continue;
-            const bool live = it.has_work && ok && kj < it.s.len_kv;
-            const bool row_in_slot = kj < it.s.slot_kv;
-            const int64_t prow = it.s.kv_row0 + kj;
-            const int which = half;
-            {
-                const uint32_t col = tmem + (which == 0 ? C::kColDV : C::kColDK);
-                const float mul = which == 0 ? 1.f : a.scale;
+            constexpr int kCpr = HD / 8;       // 16-byte chunks per row
+            const bool have = it.has_work && ok;  // uniform over the 256 threads
+            const uint32_t stg_base = (C::kAhead ? C::kDS + ((q_it + C::kDsBufs - 1) % C::kDsBufs) * 32768u : C::kP) +
+                                      half * (128 * HD * 2);
+            uint8_t* stg = sm + stg_base;
+            const bool use_tma = !thd || it.kv_base + kTileKV <= it.s.slot_kv;
+            const int64_t* sst = half == 0 ? a.dv_stride : a.dk_stride;
+            uint16_t* base = static_cast<uint16_t*>(half == 0 ? a.dv : a.dk);
+            if (have) {
+                const uint32_t col = tmem + (half == 0 ? C::kColDV : C::kColDK);
+                const float mul = half == 0 ? 1.f : a.scale;
+                const bool live = kj < it.s.len_kv;
 #pragma unroll 1
-                for (int ch = 0; ch < HD / 16; ++ch) {
-                    uint32_t v[16];
-                    if (it.has_work && ok) {
-                        tmem_ld16(col + lane_off + ch * 16, v);
-                        tmem_ld_wait();
-                    }
-                    float f[16];
+                for (int blk = 0; blk < HD / 32; ++blk) {
+                    uint32_t v[32];
+                    tmem_ld32(col + lane_off + blk * 32, v);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) f[e] = live ? __uint_as_float(v[e]) * mul : 0.f;
-                    if (!row_in_slot) continue;
-                    {
-                        const int64_t* sst = which == 0 ? a.dv_stride : a.dk_stride;
-                        uint16_t* base = static_cast<uint16_t*>(which == 0 ? a.dv : a.dk);
-                        uint16_t* dst = base + (thd ? prow * sst[1] : it.bi * sst[0] + kj * sst[1]) +
-                                        it.gk * sst[2] + ch * 16;
+                    for (int c = 0; c < 4; ++c) {
+                        float f[8];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 8)
-                            *reinterpret_cast<uint4*>(dst + e) =
-                                make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
-                                           pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
+                        for (int e = 0; e < 8; ++e) f[e] = live ? __uint_as_float(v[8 * c + e]) * mul : 0.f;
+                        *reinterpret_cast<uint4*>(stg + stg_off(r, blk * 4 + c)) =
+                            make_uint4(pack2<BF16>(f[0], f[1]), pack2<BF16>(f[2], f[3]),
+                                       pack2<BF16>(f[4], f[5]), pack2<BF16>(f[6], f[7]));
                     }
                 }
-            }
-            if (it.has_work && ok) {
                 tc_fence_before();
                 mbar_arrive(bar(kAccEmpty));
+                if (use_tma) fence_proxy_async_smem();
+                named_bar_sync(kBarSoft, kSoftThreads);
+                if (use_tma) {
+                    if (r == 0) {
+                        const int kvrow = static_cast<int>((thd ? it.s.kv_row0 : 0) + it.kv_base);
+#pragma unroll
+                        for (int cb = 0; cb < HD / 64; ++cb)
+                            tma_put(false, thd, half == 0 ? &a.tm_dv : &a.tm_dk, sbase + stg_base + cb * kBlock16K,
+                                    cb * 64, static_cast<int>(it.gk), kvrow, static_cast<int>(it.bi));
+                        bulk_commit();
+                    }
+                    store_buf = static_cast<int>((q_it + C::kDsBufs - 1) % C::kDsBufs);
+                    if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                        SWA_TRACE(warp == kWarpSoft0 ? 18 : 19, q_it - 1);
+                    continue;
+                }
+            }
+            // row-wise: HD/8 threads per row
+            {
+                const int c = r % kCpr;
+#pragma unroll 1
+                for (int pass = 0; pass < kCpr; ++pass) {
+                    const int row = pass * (128 / kCpr) + r / kCpr;
+                    const int64_t kr = it.kv_base + row;
+                    if (kr >= it.s.slot_kv) break;   // rows ascend with the pass
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (have) w = *reinterpret_cast<const uint4*>(stg + stg_off(row, c));
+                    uint16_t* dst = base + (thd ? (it.s.kv_row0 + kr) * sst[1] : it.bi * sst[0] + kr * sst[1]) +
+                                    it.gk * sst[2] + c * 8;
+                    *reinterpret_cast<uint4*>(dst) = w;
+                }
             }
         }
     } else {
@@ -573,8 +766,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         //  - otherwise (n >= 3): unordered vector atomics into the accumulator,
         //    which the preprocess zeroed for these tiles; the dQ convert
         //    kernel converts them.
+        // Each thread reads its q row (a TMEM lane) and scales it; 32 columns at
+        // a time go through a staged fp32 tile (16-byte chunk c of row r at
+        // chunk c ^ (r % 8)), from which 8 threads per row apply them to global
+        // memory, so that each warp access covers whole rows.
         const int r = tid - kWarpDq0 * 32;  // q row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint8_t* stg = sm + C::kDqStage;
+        const uint32_t stg_s = sbase + C::kDqStage;
         uint32_t dq_it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -582,72 +781,148 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             if (!it.has_work) continue;
             for (int64_t k = 0; k < it.steps; ++k) {
                 const int64_t j = it.qtile(k), hh = it.head(k);
+                if (r == 0) bulk_wait_read0();   // the staging is free again
                 if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
                 if (r == 0) SWA_TRACE(9, dq_it);
                 ++dq_it;
                 tc_fence_after();
-                const int64_t qi = j * kTileQ + r;
-                const bool row_ok = qi < it.s.len_q;
-                const int64_t prow = it.s.q_row0 + qi;
                 int64_t first, nvis;
                 q_tile_visitors(g, it.s, j, first, nvis);
                 const int turn = static_cast<int>(it.t - first);
                 const bool single = nvis <= 1;
                 int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
-                float* acc = a.dq_acc + (prow * g.h_q + hh) * HD;
-                uint16_t* dqp = static_cast<uint16_t*>(a.dq) +
-                                (thd ? prow * a.dq_stride[1] : it.bi * a.dq_stride[0] + qi * a.dq_stride[1]) +
-                                hh * a.dq_stride[2];
                 // two visitors, or deterministic mode: hand the tile along in turn order
                 const bool relay = a.deterministic || nvis == 2;
                 const bool accumulate = !single && !relay;
                 const bool conv_now = single || (relay && turn == nvis - 1);
-                // Waits for this visit's turn (relay) or for the first visitor's store.
+                // accumulator write: a store for the first relay turn, else an add
+                const bool add = !(relay && turn == 0);
+                // TMA writes whole 128-row boxes: the tile must lie inside the
+                // sequence's slot (always so for BSHD, whose maps end at s_q)
+                const bool use_tma = !thd || (j + 1) * kTileQ <= it.s.slot_q;
+                const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
+                const int tb = static_cast<int>(it.bi), th = static_cast<int>(hh);
+                // Waits for this visit's turn (relay) in thread 0; true in all 128
+                // threads if the turn came (or none was needed) and nothing aborted.
                 auto wait_turn = [&]() -> bool {
-                    if (!relay || turn == 0) return true;
-                    if (r == 0) {
+                    bool mine = true;
+                    if (relay && turn > 0 && r == 0) {
                         const uint64_t t0 = globaltimer_ns();
                         for (;;) {
                             if (ld_acquire_gpu(sem) == turn) break;
                             if (*abort_flag || globaltimer_ns() - t0 > tmo) {
                                 set_status(a.status, kStatusTimeout);
                                 *abort_flag = 1;
+                                mine = false;
                                 break;
                             }
                         }
+                        // later async-proxy writes follow the acquired ones
+                        fence_proxy_async_global();
                     }
-                    named_bar_sync(kBarDq, 128);
-                    return *abort_flag == 0;
+                    return bar_and(kBarDq, 128, mine && *abort_flag == 0);
                 };
-                // Writes 32 dQ values of this row: converted (plus the partial sum
-                // of the earlier visitors unless alone), stored as the first
-                // partial, or added to it.
-                auto emit = [&](int col, float (&f)[32]) {
-                    if (conv_now) {
-                        if (!single) {
+                // Converts 32 dQ values of this row (columns [32 ch, 32 ch + 32)),
+                // adding the earlier visitors' partial sum unless alone, into the
+                // staged 16-bit tile.
+                auto stage_out = [&](int ch, const uint32_t (&v)[32]) {
+                    float f[32];
 #pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                const float4 o = ld_cg_f4(acc + col + e);
-                                f[e] += o.x; f[e + 1] += o.y; f[e + 2] += o.z; f[e + 3] += o.w;
+                    for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * a.scale;
+                    if (!single) {
+                        // rows past the sequence's length hold zeros and take none
+                        // (their load reads the last row instead, a valid address)
+                        const int64_t qi = j * kTileQ + r;
+                        const bool row_ok = qi < it.s.len_q;
+                        const float* accr =
+                            a.dq_acc + ((it.s.q_row0 + (row_ok ? qi : it.s.len_q - 1)) * g.h_q + hh) * HD + ch * 32;
+                        const float m = row_ok ? 1.f : 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 o = ld_cg_f4(accr + e);
+                            f[e] += m * o.x; f[e + 1] += m * o.y; f[e + 2] += m * o.z; f[e + 3] += m * o.w;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<uint4*>(stg + stg_off(r, ch * 4 + i)) =
+                            make_uint4(pack2<BF16>(f[8 * i], f[8 * i + 1]), pack2<BF16>(f[8 * i + 2], f[8 * i + 3]),
+                                       pack2<BF16>(f[8 * i + 4], f[8 * i + 5]),
+                                       pack2<BF16>(f[8 * i + 6], f[8 * i + 7]));
+                };
+                // Stages 32 fp32 values of this row as chunks [8 blk, 8 blk + 8).
+                auto stage_acc = [&](int blk, const uint32_t (&v)[32]) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(stg + stg_off(r, blk * 8 + i)) =
+                            make_float4(__uint_as_float(v[4 * i]) * a.scale, __uint_as_float(v[4 * i + 1]) * a.scale,
+                                        __uint_as_float(v[4 * i + 2]) * a.scale,
+                                        __uint_as_float(v[4 * i + 3]) * a.scale);
+                };
+                // Writes the staged fp32 columns [col0, col0 + 64) of the tile
+                // from thread 0 with two TMA boxes.
+                auto put_acc = [&](int col0) {
+                    fence_proxy_async_smem();
+                    named_bar_sync(kBarDq, 128);
+                    if (r == 0) {
+                        tma_put(add, thd, &a.tm_acc, stg_s, col0, th, qrow, tb);
+                        tma_put(add, thd, &a.tm_acc, stg_s + kBlock16K, col0 + 32, th, qrow, tb);
+                        bulk_commit();
+                    }
+                };
+                // Row-wise fallback for a tile that ends past its sequence's slot
+                // (THD): applies staged fp32 columns [col0, col0 + 64) with 16
+                // threads per row -- converted (plus the earlier visitors' sum
+                // unless alone), stored as the first partial, or added to it.
+                // Partial sums are loaded 8 rows at a time before any store.
+                auto apply = [&](int col0) {
+                    named_bar_sync(kBarDq, 128);
+                    const int c = r & 15, col = col0 + c * 4;
+                    const int64_t qi0 = j * kTileQ + (r >> 4);   // pass p: row (r >> 4) + 8 p
+                    const int64_t nrows = it.s.len_q - qi0;     // passes with 8 p < nrows run
+                    float* acc0 = a.dq_acc + ((it.s.q_row0 + qi0) * g.h_q + hh) * HD + col;
+                    const int64_t acc_step = 8 * g.h_q * HD;
+                    // last row of the sequence, a valid address for every pass's load
+                    float* acc_last = a.dq_acc + ((it.s.q_row0 + it.s.len_q - 1) * g.h_q + hh) * HD + col;
+#pragma unroll
+                    for (int p0 = 0; p0 < 16; p0 += 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            v[u] = *reinterpret_cast<const float4*>(stg + stg_off((p0 + u) * 8 + (r >> 4), c));
+                        if (conv_now && !single) {
+                            float4 o[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                o[u] = ld_cg_f4((p0 + u) * 8 < nrows ? acc0 + (p0 + u) * acc_step : acc_last);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                v[u].x += o[u].x; v[u].y += o[u].y; v[u].z += o[u].z; v[u].w += o[u].w;
                             }
                         }
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8)
-                            *reinterpret_cast<uint4*>(dqp + col + e) =
-                                make_uint4(pack2<BF16>(f[e], f[e + 1]), pack2<BF16>(f[e + 2], f[e + 3]),
-                                           pack2<BF16>(f[e + 4], f[e + 5]), pack2<BF16>(f[e + 6], f[e + 7]));
-                    } else if (turn == 0 && !accumulate) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(acc + col + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) red_add_v4(acc + col + e, f[e], f[e + 1], f[e + 2], f[e + 3]);
+                        for (int u = 0; u < 8; ++u) {
+                            if ((p0 + u) * 8 >= nrows) break;
+                            float* accp = acc0 + (p0 + u) * acc_step;
+                            if (conv_now) {
+                                const int64_t qi = qi0 + (p0 + u) * 8, prow = it.s.q_row0 + qi;
+                                uint16_t* dqp = static_cast<uint16_t*>(a.dq) +
+                                                (thd ? prow * a.dq_stride[1]
+                                                     : it.bi * a.dq_stride[0] + qi * a.dq_stride[1]) +
+                                                hh * a.dq_stride[2] + col;
+                                *reinterpret_cast<uint2*>(dqp) =
+                                    make_uint2(pack2<BF16>(v[u].x, v[u].y), pack2<BF16>(v[u].z, v[u].w));
+                            } else if (!add) {
+                                *reinterpret_cast<float4*>(accp) = v[u];
+                            } else {
+                                red_add_v4(accp, v[u].x, v[u].y, v[u].z, v[u].w);
+                            }
+                        }
                     }
                 };
-                bool turn_ok = true;
+                bool go;
                 if constexpr (HD == 64) {
-                    // the whole row fits in registers: free TMEM before any wait
+                    // read the whole row and free TMEM before any wait
                     uint32_t v0[32], v1[32];
                     tmem_ld32(tmem + C::kColDQ + lane_off, v0);
                     tmem_ld32(tmem + C::kColDQ + lane_off + 32, v1);
@@ -655,41 +930,101 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     tc_fence_before();
                     mbar_arrive(bar(kDqEmpty));
                     if (r == 0) SWA_TRACE(10, dq_it - 1);
-                    float f0[32], f1[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        f0[e] = __uint_as_float(v0[e]) * a.scale;
-                        f1[e] = __uint_as_float(v1[e]) * a.scale;
-                    }
-                    turn_ok = wait_turn();
-                    if (row_ok && turn_ok) {
-                        emit(0, f0);
-                        emit(32, f1);
+                    go = wait_turn();
+                    if (r == 0) SWA_TRACE(15, dq_it - 1);
+                    if (go) {
+                        if (conv_now && use_tma) {
+                            stage_out(0, v0);
+                            stage_out(1, v1);
+                            fence_proxy_async_smem();
+                            named_bar_sync(kBarDq, 128);
+                            if (r == 0) {
+                                tma_put(false, thd, &a.tm_dq, stg_s, 0, th, qrow, tb);
+                                bulk_commit();
+                            }
+                        } else {
+                            stage_acc(0, v0);
+                            stage_acc(1, v1);
+                            if (use_tma) put_acc(0);
+                            else apply(0);
+                        }
                     }
                 } else {
-                    turn_ok = wait_turn();
+                    go = wait_turn();
+                    if (r == 0) SWA_TRACE(15, dq_it - 1);
+                    // With a partial sum to add, the row-wise path loads it eight
+                    // rows at a time; read per row here, its latency would hold
+                    // the dQ columns of TMEM (aliasing S^T) four times over.
+                    if (conv_now && use_tma && single) {
 #pragma unroll 1
-                    for (int ch = 0; ch < HD / 32; ++ch) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + C::kColDQ + lane_off + ch * 32, v);
-                        tmem_ld_wait();
-                        float f[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * a.scale;
-                        if (row_ok && turn_ok) emit(ch * 32, f);
+                        for (int ch = 0; ch < HD / 32; ++ch) {
+                            uint32_t v[32];
+                            tmem_ld32(tmem + C::kColDQ + lane_off + ch * 32, v);
+                            tmem_ld_wait();
+                            if (go) stage_out(ch, v);
+                        }
+                        tc_fence_before();
+                        mbar_arrive(bar(kDqEmpty));
+                        fence_proxy_async_smem();
+                        named_bar_sync(kBarDq, 128);
+                        if (r == 0 && go) {
+                            tma_put(false, thd, &a.tm_dq, stg_s, 0, th, qrow, tb);
+                            tma_put(false, thd, &a.tm_dq, stg_s + kBlock16K, 64, th, qrow, tb);
+                            bulk_commit();
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int rd = 0; rd < HD / 64; ++rd) {
+                            if (rd > 0) {
+                                // the previous half has left the staging
+                                if (r == 0) bulk_wait_read0();
+                                named_bar_sync(kBarDq, 128);
+                            }
+                            uint32_t v[32];
+                            tmem_ld32(tmem + C::kColDQ + lane_off + rd * 64, v);
+                            tmem_ld_wait();
+                            stage_acc(0, v);
+                            tmem_ld32(tmem + C::kColDQ + lane_off + rd * 64 + 32, v);
+                            tmem_ld_wait();
+                            stage_acc(1, v);
+                            if (use_tma && !conv_now) {
+                                fence_proxy_async_smem();
+                                named_bar_sync(kBarDq, 128);
+                                if (r == 0 && go) {
+                                    tma_put(add, thd, &a.tm_acc, stg_s, rd * 64, th, qrow, tb);
+                                    tma_put(add, thd, &a.tm_acc, stg_s + kBlock16K, rd * 64 + 32, th, qrow, tb);
+                                    bulk_commit();
+                                }
+                            } else if (go) {
+                                apply(rd * 64);
+                            } else {
+                                named_bar_sync(kBarDq, 128);
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(bar(kDqEmpty));
                     }
-                    tc_fence_before();
-                    mbar_arrive(bar(kDqEmpty));
                 }
                 if (r == 0) SWA_TRACE(11, dq_it - 1);
-                if (!relay) continue;
-                // publish: the group's writes are ordered before one release
-                named_bar_sync(kBarDq, 128);
-                if (r == 0 && turn + 1 < nvis) st_release_gpu(sem, turn + 1);
+                if (!relay || turn + 1 >= nvis) continue;
+                // publish this turn's partial sum to the next visitor
+                if (use_tma) {
+                    // thread 0 issued every copy of the tile: complete them first
+                    if (r == 0) {
+                        bulk_wait0();
+                        fence_proxy_async_global();
+                        st_release_gpu(sem, turn + 1);
+                    }
+                } else {
+                    // the group's stores are ordered before one release
+                    named_bar_sync(kBarDq, 128);
+                    if (r == 0) st_release_gpu(sem, turn + 1);
+                }
             }
         }
     }
 
+    bulk_wait0();   // copies issued from this CTA's shared memory are complete
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {
@@ -702,7 +1037,7 @@ template <int HD, bool BF16>
 static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 {
     auto kern = sdpa_bwd_main_kernel<HD, BF16>;
-    const uint32_t bytes = Cfg<HD>::kAlloc;
+    const uint32_t bytes = Cfg<HD>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     const int64_t items = a.g.b * a.g.h_kv * a.n_kv_tiles;

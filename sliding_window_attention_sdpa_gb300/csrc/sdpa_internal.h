@@ -13,7 +13,8 @@ namespace swa {
 constexpr int kTileKV = 128;      // kv rows per CTA work item (MMA M of dK/dV side)
 constexpr int kTileQ = 128;       // q rows per inner-loop step
 constexpr int kPreRows = 64;      // token rows per preprocess CTA
-constexpr int kStatusTimeout = 4; // same codes as sdpa_status_t
+constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
+constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;
 
 // Workspace layout (byte offsets from the workspace base, 256-B aligned).
@@ -64,6 +65,10 @@ struct MainArgs {
     // TMA descriptors of Q, K, V, dO: BSHD 4-D (d, h, s, b), THD 3-D (d, h, t);
     // 64 x 1 x 128 boxes with the 128-byte swizzle.
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    // Output descriptors for TMA stores from staged tiles: dQ, dK, dV (I/O
+    // dtype, 64 x 1 x 128 boxes) and the fp32 dQ accumulator (32 x 1 x 128
+    // boxes), all with the 128-byte swizzle.
+    CUtensorMap tm_dq, tm_dk, tm_dv, tm_acc;
     Geometry g;
     const void *q, *k, *v, *dout;
     const float2* stats;      // per-row (LSE * log2(e), D), tile-aligned (see PreArgs)
