@@ -182,7 +182,7 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "1632ef6bc26c1423", "bytes": 250243840},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "ee896f262549ad28", "bytes": 251209472},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 

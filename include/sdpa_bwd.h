@@ -170,7 +170,9 @@ sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace
 /*
  * Synchronises `stream` and returns the device status word of the last
  * backward run on `workspace`: SDPA_OK, SDPA_ERR_TIMEOUT (a relay wait gave up;
- * dQ is then incomplete) or SDPA_ERR_BAD_LENGTHS.
+ * dQ is then incomplete), SDPA_ERR_BAD_LENGTHS, or SDPA_ERR_UNSUPPORTED (the
+ * device placed the main kernel's dynamic shared memory off a 1024-byte
+ * boundary, which its swizzled tiles need; it then computed nothing).
  */
 sdpa_status_t sdpa_bwd_check_status(const void *workspace, void *stream);
 
