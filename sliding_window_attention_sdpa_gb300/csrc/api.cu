@@ -74,6 +74,11 @@ sdpa_status_t check_shape(const sdpa_bwd_params* p)
                     (long long)p->s_q, (long long)p->s_kv);
     if ((p->sink == nullptr) != (p->dsink == nullptr))
         return fail(SDPA_ERR_INVALID_ARG, "sink and dsink must both be set or both be NULL");
+    // the main kernel numbers its work items (b x h_kv x kv-tiles) in 32 bits
+    const int64_t n_items = p->b * p->h_kv * ((p->s_kv + swa::kTileKV - 1) / swa::kTileKV);
+    if (n_items >= (int64_t(1) << 31))
+        return fail(SDPA_ERR_UNSUPPORTED, "%lld work items (b x h_kv x ceil(s_kv/128)): at most 2^31 - 1",
+                    (long long)n_items);
     return SDPA_OK;
 }
 

@@ -275,12 +275,27 @@ struct Item {
     int64_t nq, steps;   // q-tiles per head, steps = group * nq
     bool has_work;       // at least one q-tile to sweep
     bool in_slot;        // the kv-tile has rows inside the sequence's slot
-    // step k: q-head h0 + k / nq, q-tile q_hi - 1 - k % nq
-    __device__ __forceinline__ int64_t head(int64_t k) const { return h0 + k / nq; }
-    __device__ __forceinline__ int64_t qtile(int64_t k) const { return q_hi - 1 - k % nq; }
+    // Steps run q-head h0 .. h0 + group - 1, each over q-tiles q_hi - 1 down to
+    // q_lo; counters rather than divisions (there is no 64-bit divider, and
+    // these sit on every role's hand-off path).
+    __device__ __forceinline__ void advance(int64_t& j, int64_t& hh) const
+    {
+        if (j == q_lo) {
+            j = q_hi - 1;
+            ++hh;
+        } else {
+            --j;
+        }
+    }
 };
 
-__device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
+// Per-launch constants of the item numbering (32-bit: the host keeps the item
+// count below 2^31).
+struct ItemCounts {
+    uint32_t h_kv, n_kv_tiles, group;
+};
+
+__device__ __forceinline__ Item decode(const MainArgs& a, const ItemCounts& n, int64_t item)
 {
     const Geometry& g = a.g;
     Item it;
@@ -290,10 +305,12 @@ __device__ __forceinline__ Item decode(const MainArgs& a, int64_t item)
     // concentrates their loads and stores on a few memory partitions. The
     // previous kv-tile of the same head (the dQ relay partner) is then item
     // - h_kv, which runs in the same wave.
-    it.gk = item % g.h_kv;
-    it.t = (item / g.h_kv) % a.n_kv_tiles;
-    it.bi = item / (a.n_kv_tiles * g.h_kv);
-    it.group = g.h_q / g.h_kv;
+    const uint32_t u = static_cast<uint32_t>(item);
+    const uint32_t rest = u / n.h_kv, bq = rest / n.n_kv_tiles;
+    it.gk = u - rest * n.h_kv;
+    it.t = rest - bq * n.n_kv_tiles;
+    it.bi = bq;
+    it.group = n.group;
     it.h0 = it.gk * it.group;
     it.s = seq_info(g, it.bi);
     it.kv_base = it.t * kTileKV;
@@ -350,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const uint64_t tmo = static_cast<uint64_t>(a.timeout_ns);
     const int64_t n_items = g.b * g.h_kv * a.n_kv_tiles;
     const bool thd = g.layout == 1;
+    const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
+                         static_cast<uint32_t>(g.h_q / g.h_kv)};
 
     if (tid == 0) {
         misc[1] = 0;
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
             for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-                const Item it = decode(a, item);
+                const Item it = decode(a, cnt, item);
                 if (!it.has_work) continue;
                 const int ks = kv_it % C::kKvStages;
                 if (!wait(kKvEmpty0 + ks, ((kv_it / C::kKvStages) & 1) ^ 1)) break;
@@ -413,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 tma_tile<HD>(sbase + C::kV + ks * C::kTile, &a.tm_v, bar(kKvFull0 + ks), thd,
                              (int)it.gk, kvrow, (int)it.bi);
                 bool ok = true;
-                for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
-                    const int64_t j = it.qtile(k), hh = it.head(k);
+                for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
                     SWA_TRACE(12, q_it);
@@ -499,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode(a, item);
+            const Item it = decode(a, cnt, item);
             if (!it.has_work) continue;
             const int ks = kv_it % C::kKvStages;
             if (!(ok = wait_warp(kKvFull0 + ks, (kv_it / C::kKvStages) & 1))) break;
@@ -507,8 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             const uint32_t sK = sbase + C::kK + ks * C::kTile, sV = sbase + C::kV + ks * C::kTile;
             if (it.kv_base + kTileKV > it.s.len_kv)
                 zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
-            for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
-                const int64_t j = it.qtile(k);
+            for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
                 const int st = q_it % C::kStages;
                 if (!(ok = wait_warp(kQFull0 + st, (q_it / C::kStages) & 1))) break;
                 if (lane == 0) SWA_TRACE(0, q_it);
@@ -581,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-            const Item it = decode(a, item);
+            const Item it = decode(a, cnt, item);
             const int64_t kj = it.kv_base + r;
             if (r == 0 && half == 0 && it.s.bad && it.t == 0 && it.gk == 0)
                 set_status(a.status, kStatusBadLengths);
@@ -590,8 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - it.s.diag);
                 if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - it.s.diag);
                 if (kj >= it.s.len_kv) i_hi = -1;
-                for (int64_t k = 0; k < it.steps; ++k, ++q_it) {
-                    const int64_t j = it.qtile(k);
+                for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
                     const int st = q_it % C::kStages;
                     release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
                     if (!(ok = wait_group(kBarSoft, kSoftThreads, kQFull0 + st, (q_it / C::kStages) & 1))) break;
@@ -777,10 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         uint32_t dq_it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode(a, item);
+            const Item it = decode(a, cnt, item);
             if (!it.has_work) continue;
-            for (int64_t k = 0; k < it.steps; ++k) {
-                const int64_t j = it.qtile(k), hh = it.head(k);
+            for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, it.advance(j, hh)) {
                 if (r == 0) bulk_wait_read0();   // the staging is free again
                 if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
                 if (r == 0) SWA_TRACE(9, dq_it);
