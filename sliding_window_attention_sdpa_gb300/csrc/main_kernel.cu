@@ -254,7 +254,7 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool v)
 // role's hand-offs for the first kTraceCtas CTAs and kTraceTiles q-tiles, written
 // to the workspace at byte offset kTraceOffset (the caller sizes the workspace
 // for it). Off by default; it records and changes nothing else.
-constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceSlots = 20;
+constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceSlots = 24;
 constexpr size_t kTraceOffset = size_t(256) << 20;
 #ifdef SDPA_BWD_TRACE
 #define SWA_TRACE(slot, tile)                                                                    \
@@ -597,8 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             }
         };
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-            const Item it = decode(a, cnt, item);
+        // The next item is decoded right after this one's last P^T hand-off, so
+        // that its (cold) decode overlaps the wait for the last gradients.
+        auto decode_at = [&](int64_t i) -> Item { return decode(a, cnt, i < n_items ? i : blockIdx.x); };
+        Item it = decode(a, cnt, blockIdx.x), nxt;
+        bool have_nxt = false;
+        for (int64_t item = blockIdx.x; item < n_items;
+             item += gridDim.x, it = have_nxt ? nxt : decode_at(item), have_nxt = false) {
             const int64_t kj = it.kv_base + r;
             if (r == 0 && half == 0 && it.s.bad && it.t == 0 && it.gk == 0)
                 set_status(a.status, kStatusBadLengths);
@@ -609,9 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (kj >= it.s.len_kv) i_hi = -1;
                 for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
                     const int st = q_it % C::kStages;
+                    if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(20, q_it);
                     release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
-                    if (!(ok = wait_group(kBarSoft, kSoftThreads, kQFull0 + st, (q_it / C::kStages) & 1))) break;
-                    if (!(ok = wait_group(kBarSoft, kSoftThreads, kSFull, s_it & 1))) break;
+                    if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(21, q_it);
+                    // this q-tile's (LSE, D) pairs and S^T, dP^T: one group barrier
+                    if (!(ok = bar_and(kBarSoft, kSoftThreads,
+                                       wait(kQFull0 + st, (q_it / C::kStages) & 1) && wait(kSFull, s_it & 1))))
+                        break;
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
                         SWA_TRACE(warp == kWarpSoft0 ? 5 : 7, q_it);
                     ++s_it;
@@ -694,6 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
                         SWA_TRACE(warp == kWarpSoft0 ? 6 : 8, q_it);
                 }
+                nxt = decode_at(item + gridDim.x);
+                have_nxt = true;
                 release_buf(static_cast<int>((q_it + C::kDsBufs - 1) % C::kDsBufs));   // the epilogue's staging
                 if (ok) ok = wait_group(kBarSoft, kSoftThreads, kAccFull, acc_it & 1);
                 if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
