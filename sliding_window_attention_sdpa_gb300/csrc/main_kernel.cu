@@ -479,9 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 SWA_TRACE(3, p.q_it);
                 tc_fence_after();
                 const uint32_t acc = p.first ? 0u : 1u;
+                // K-major (16, 1024) and MN-major (16 KB, 1024) descriptors of the
+                // operand tiles; each contraction step adds its byte offset
+                const uint64_t dDOmn = sdesc_sw128(sDO, kBlock16K, 1024), dQmn = sdesc_sw128(sQ, kBlock16K, 1024);
+                const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024);
+                const uint64_t dDSk = sdesc_sw128(sDS, 16, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint64_t bdesc = sdesc_sw128(sDO + k * 2048, kBlock16K, 1024);
+                    const uint64_t bdesc = sdesc_at(dDOmn, k * 2048);
                     if constexpr (C::kPInTmem) {
                         umma_f16_ts(tm_dv, tmem + C::kColP + k * 8, bdesc, kIdPV, acc | (k > 0));
                     } else {
@@ -496,13 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                    umma_f16_ss(tm_dk, sdesc_sw128(sDS + aoff, 16, 1024),
-                                sdesc_sw128(sQ + k * 2048, kBlock16K, 1024), kIdPV, acc | (k > 0));
+                    umma_f16_ss(tm_dk, sdesc_at(dDSk, aoff), sdesc_at(dQmn, k * 2048), kIdPV, acc | (k > 0));
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    umma_f16_ss(tm_dq, sdesc_sw128(sDS + k * 2048, kBlock16K, 1024),
-                                sdesc_sw128(sK + k * 2048, kBlock16K, 1024), kIdDQ, k > 0);
+                    umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ, k > 0);
                 umma_commit(bar(kDqFull));
                 umma_commit(bar(kQEmpty0 + p.st));
                 SWA_TRACE(4, p.q_it);
@@ -546,17 +549,17 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const uint32_t sQ = sbase + C::kQ + st * C::kTile, sDO = sbase + C::kDO + st * C::kTile;
                 if (lane == 0) {
                     tc_fence_after();
+                    const uint64_t dK = sdesc_sw128(sK, 16, 1024), dQ = sdesc_sw128(sQ, 16, 1024);
+                    const uint64_t dV = sdesc_sw128(sV, 16, 1024), dDO = sdesc_sw128(sDO, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < HD / 16; ++k) {
                         const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_s, sdesc_sw128(sK + koff, 16, 1024),
-                                    sdesc_sw128(sQ + koff, 16, 1024), kIdQK, k > 0);
+                        umma_f16_ss(tm_s, sdesc_at(dK, koff), sdesc_at(dQ, koff), kIdQK, k > 0);
                     }
 #pragma unroll
                     for (int k = 0; k < HD / 16; ++k) {
                         const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dp, sdesc_sw128(sV + koff, 16, 1024),
-                                    sdesc_sw128(sDO + koff, 16, 1024), kIdQK, k > 0);
+                        umma_f16_ss(tm_dp, sdesc_at(dV, koff), sdesc_at(dDO, koff), kIdQK, k > 0);
                     }
                     umma_commit(bar(kSFull));
                     SWA_TRACE(1, q_it);

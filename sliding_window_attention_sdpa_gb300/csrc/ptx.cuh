@@ -222,6 +222,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The descriptor of saddr + off, from that of saddr: the start field holds
+// addresses up to 256 KB, so adding off >> 4 never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t desc, uint32_t off)
+{
+    return desc + (off >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
 // Bits: [4,6) D format (1 = f32), [7,10) A format, [10,13) B format
 // (0 = f16, 1 = bf16), 15 A MN-major, 16 B MN-major, [17,23) N>>3, [24,29) M>>4.
