@@ -90,8 +90,8 @@ struct Cfg {
     static constexpr uint32_t kDqStage = kDS + kDsBufs * 32768;
     static constexpr uint32_t kStat = kDqStage + 128 * kDqCols * 4;  // kStages x 128 float2
     static constexpr uint32_t kBars = kStat + kStages * 1024;   // mbarriers
-    static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags
-    static constexpr uint32_t kBytes = kMisc + 64;
+    static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags, deferred epilogue
+    static constexpr uint32_t kBytes = kMisc + 128;
     static_assert(kBytes <= 232448, "shared memory above the 227 KB a CTA may opt into");
     // The dK/dV epilogue stages two 128 x HD 16-bit tiles (2 x 16 KB at d = 64,
     // 2 x 32 KB at d = 128) in a dS^T buffer (d = 64) or in the P^T + dS^T
@@ -287,6 +287,16 @@ struct Item {
             --j;
         }
     }
+};
+
+// One work item's dK/dV store, as the softmax group runs it (d = 64 defers it
+// to after the next item's first q-tile, keeping it in shared memory).
+struct Epi {
+    int64_t kv_base, kv_row0, len_kv, slot_kv, bi, gk;
+    uint32_t acc_par;   // parity of the item's acc-full phase
+    int32_t buf;        // dS^T buffer to stage in (d = 64)
+    int32_t have;       // TMEM holds the item's dK/dV (else the rows are zero)
+    int32_t last;       // the item's last step (trace index)
 };
 
 // Per-launch constants of the item numbering (32-bit: the host keeps the item
@@ -600,6 +610,83 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             }
         };
         bool ok = true;
+        Epi* epi_slot = reinterpret_cast<Epi*>(sm + C::kMisc + 16);
+        bool epi_pending = false;   // an item's dK/dV store waits in epi_slot
+        // Epilogue of one item: half 0 writes the tile's dV, half 1 its dK
+        // (scaled). Each thread converts its kv row from TMEM into a staged
+        // 16-bit tile (128-byte-swizzle layout), which one thread stores with TMA;
+        // a tile ending past its sequence's slot (THD) is stored row-wise instead.
+        // Rows past the sequence's length are zero; rows past its slot (or past
+        // s_kv, where the BSHD maps end) are not written.
+        auto run_epi = [&](const Epi e) {
+            constexpr int kCpr = HD / 8;   // 16-byte chunks per row
+            const int64_t kj = e.kv_base + r;
+            bool have = e.have != 0;
+            if (have) {
+                release_buf(e.buf);   // ordered by the barrier below
+                ok = wait_group(kBarSoft, kSoftThreads, kAccFull, e.acc_par);
+                have = ok;
+                if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                    SWA_TRACE(warp == kWarpSoft0 ? 16 : 17, e.last);
+                if (ok) tc_fence_after();
+            }
+            const uint32_t stg_base = (C::kAhead ? C::kDS + e.buf * 32768u : C::kP) + half * (128 * HD * 2);
+            uint8_t* stg = sm + stg_base;
+            const bool use_tma = !thd || e.kv_base + kTileKV <= e.slot_kv;
+            const int64_t* sst = half == 0 ? a.dv_stride : a.dk_stride;
+            uint16_t* base = static_cast<uint16_t*>(half == 0 ? a.dv : a.dk);
+            if (have) {
+                const uint32_t col = tmem + (half == 0 ? C::kColDV : C::kColDK);
+                const float mul = half == 0 ? 1.f : a.scale;
+                const bool live = kj < e.len_kv;
+#pragma unroll 1
+                for (int blk = 0; blk < HD / 32; ++blk) {
+                    uint32_t v[32];
+                    tmem_ld32(col + lane_off + blk * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float f[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) f[x] = live ? __uint_as_float(v[8 * c + x]) * mul : 0.f;
+                        *reinterpret_cast<uint4*>(stg + stg_off(r, blk * 4 + c)) =
+                            make_uint4(pack2<BF16>(f[0], f[1]), pack2<BF16>(f[2], f[3]),
+                                       pack2<BF16>(f[4], f[5]), pack2<BF16>(f[6], f[7]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(kAccEmpty));
+                if (use_tma) fence_proxy_async_smem();
+                named_bar_sync(kBarSoft, kSoftThreads);
+                if (use_tma) {
+                    if (r == 0) {
+                        const int kvrow = static_cast<int>((thd ? e.kv_row0 : 0) + e.kv_base);
+#pragma unroll
+                        for (int cb = 0; cb < HD / 64; ++cb)
+                            tma_put(false, thd, half == 0 ? &a.tm_dv : &a.tm_dk, sbase + stg_base + cb * kBlock16K,
+                                    cb * 64, static_cast<int>(e.gk), kvrow, static_cast<int>(e.bi));
+                        bulk_commit();
+                    }
+                    store_buf = e.buf;
+                    if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
+                        SWA_TRACE(warp == kWarpSoft0 ? 18 : 19, e.last);
+                    return;
+                }
+            }
+            // row-wise: HD/8 threads per row
+            const int c = r % kCpr;
+#pragma unroll 1
+            for (int pass = 0; pass < kCpr; ++pass) {
+                const int row = pass * (128 / kCpr) + r / kCpr;
+                const int64_t kr = e.kv_base + row;
+                if (kr >= e.slot_kv) break;   // rows ascend with the pass
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (have) w = *reinterpret_cast<const uint4*>(stg + stg_off(row, c));
+                uint16_t* dst = base + (thd ? (e.kv_row0 + kr) * sst[1] : e.bi * sst[0] + kr * sst[1]) +
+                                e.gk * sst[2] + c * 8;
+                *reinterpret_cast<uint4*>(dst) = w;
+            }
+        };
         // The next item is decoded right after this one's last P^T hand-off, so
         // that its (cold) decode overlaps the wait for the last gradients.
         auto decode_at = [&](int64_t i) -> Item { return decode(a, cnt, i < n_items ? i : blockIdx.x); };
@@ -705,84 +792,33 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     mbar_arrive(bar(kPFull));
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
                         SWA_TRACE(warp == kWarpSoft0 ? 6 : 8, q_it);
+                    if (epi_pending) {
+                        // the previous item's dK/dV store, deferred to here
+                        epi_pending = false;
+                        run_epi(*epi_slot);
+                    }
                 }
                 nxt = decode_at(item + gridDim.x);
                 have_nxt = true;
-                release_buf(static_cast<int>((q_it + C::kDsBufs - 1) % C::kDsBufs));   // the epilogue's staging
-                if (ok) ok = wait_group(kBarSoft, kSoftThreads, kAccFull, acc_it & 1);
-                if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
-                    SWA_TRACE(warp == kWarpSoft0 ? 16 : 17, q_it - 1);
-                ++acc_it;
-                if (ok) tc_fence_after();
             }
-            // Epilogue: half 0 writes the tile's dV, half 1 its dK (scaled). Each
-            // thread converts its kv row from TMEM into a staged 16-bit tile
-            // (128-byte-swizzle layout), which one thread stores with TMA; a tile
-            // ending past its sequence's slot (THD) is stored row-wise instead.
-            // Rows past the sequence's length are zero; rows past its slot (or
-            // past s_kv, where the BSHD maps end) are not written.
             if (!it.in_slot) continue;
-            constexpr int kCpr = HD / 8;       // 16-byte chunks per row
-            const bool have = it.has_work && ok;  // uniform over the 256 threads
-            const uint32_t stg_base = (C::kAhead ? C::kDS + ((q_it + C::kDsBufs - 1) % C::kDsBufs) * 32768u : C::kP) +
-                                      half * (128 * HD * 2);
-            uint8_t* stg = sm + stg_base;
-            const bool use_tma = !thd || it.kv_base + kTileKV <= it.s.slot_kv;
-            const int64_t* sst = half == 0 ? a.dv_stride : a.dk_stride;
-            uint16_t* base = static_cast<uint16_t*>(half == 0 ? a.dv : a.dk);
-            if (have) {
-                const uint32_t col = tmem + (half == 0 ? C::kColDV : C::kColDK);
-                const float mul = half == 0 ? 1.f : a.scale;
-                const bool live = kj < it.s.len_kv;
-#pragma unroll 1
-                for (int blk = 0; blk < HD / 32; ++blk) {
-                    uint32_t v[32];
-                    tmem_ld32(col + lane_off + blk * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = live ? __uint_as_float(v[8 * c + e]) * mul : 0.f;
-                        *reinterpret_cast<uint4*>(stg + stg_off(r, blk * 4 + c)) =
-                            make_uint4(pack2<BF16>(f[0], f[1]), pack2<BF16>(f[2], f[3]),
-                                       pack2<BF16>(f[4], f[5]), pack2<BF16>(f[6], f[7]));
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(bar(kAccEmpty));
-                if (use_tma) fence_proxy_async_smem();
-                named_bar_sync(kBarSoft, kSoftThreads);
-                if (use_tma) {
-                    if (r == 0) {
-                        const int kvrow = static_cast<int>((thd ? it.s.kv_row0 : 0) + it.kv_base);
-#pragma unroll
-                        for (int cb = 0; cb < HD / 64; ++cb)
-                            tma_put(false, thd, half == 0 ? &a.tm_dv : &a.tm_dk, sbase + stg_base + cb * kBlock16K,
-                                    cb * 64, static_cast<int>(it.gk), kvrow, static_cast<int>(it.bi));
-                        bulk_commit();
-                    }
-                    store_buf = static_cast<int>((q_it + C::kDsBufs - 1) % C::kDsBufs);
-                    if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
-                        SWA_TRACE(warp == kWarpSoft0 ? 18 : 19, q_it - 1);
-                    continue;
-                }
+            const Epi e{it.kv_base, it.s.kv_row0, it.s.len_kv, it.s.slot_kv, it.bi, it.gk, acc_it & 1,
+                        static_cast<int32_t>((q_it + C::kDsBufs - 1) % C::kDsBufs),
+                        static_cast<int32_t>(it.has_work && ok), static_cast<int32_t>(q_it - 1)};
+            if (it.has_work) ++acc_it;
+            if (C::kAhead && e.have) {
+                // run after the next item's first q-tile, when these gradients
+                // are long done (the next item's first gradient contractions
+                // wait for it)
+                if (r == 0 && half == 0) *epi_slot = e;
+                epi_pending = true;
+            } else {
+                run_epi(e);
             }
-            // row-wise: HD/8 threads per row
-            {
-                const int c = r % kCpr;
-#pragma unroll 1
-                for (int pass = 0; pass < kCpr; ++pass) {
-                    const int row = pass * (128 / kCpr) + r / kCpr;
-                    const int64_t kr = it.kv_base + row;
-                    if (kr >= it.s.slot_kv) break;   // rows ascend with the pass
-                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                    if (have) w = *reinterpret_cast<const uint4*>(stg + stg_off(row, c));
-                    uint16_t* dst = base + (thd ? (it.s.kv_row0 + kr) * sst[1] : it.bi * sst[0] + kr * sst[1]) +
-                                    it.gk * sst[2] + c * 8;
-                    *reinterpret_cast<uint4*>(dst) = w;
-                }
-            }
+        }
+        if (epi_pending) {
+            named_bar_sync(kBarSoft, kSoftThreads);   // epi_slot's write is visible
+            run_epi(*epi_slot);
         }
     } else {
         // ------------------------------------------------------------ dQ
