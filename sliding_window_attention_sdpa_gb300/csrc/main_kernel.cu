@@ -109,7 +109,7 @@ struct Cfg {
 // mbarrier indices
 enum Bar : int {
     kSFull = 0, kPFull, kPEmpty, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
-    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kNumBars
+    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kDqLoad, kNumBars
 };
 
 template <bool BF16>
@@ -215,6 +215,14 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 __device__ __forceinline__ uint32_t stg_off(int r, int c)
 {
     return static_cast<uint32_t>((c >> 3) * kBlock16K + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// One 128-row box of a head-strided tensor map at column c0 (see tma_put).
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool thd, int c0,
+                                        int head, int row, int batch)
+{
+    if (thd) tma_load_3d(dst, map, bar, c0, head, row);
+    else tma_load_4d(dst, map, bar, c0, head, row, batch);
 }
 
 // Loads rows [row, row + 128) of one head of a [., HD] tensor into a swizzled tile
@@ -393,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         mbar_init(bar(kDqEmpty), 128);
         mbar_init(bar(kAccFull), 1);
         mbar_init(bar(kAccEmpty), kSoftThreads);
+        mbar_init(bar(kDqLoad), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(kQFull0 + s), 1);
             mbar_init(bar(kQEmpty0 + s), 1);
@@ -840,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint8_t* stg = sm + C::kDqStage;
         const uint32_t stg_s = sbase + C::kDqStage;
-        uint32_t dq_it = 0;
+        uint32_t dq_it = 0, ld_it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode(a, cnt, item);
@@ -998,7 +1007,43 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     go = wait_turn();
                     if (r == 0) SWA_TRACE(15, dq_it - 1);
                     if (go) {
-                        if (conv_now && use_tma) {
+                        if (conv_now && use_tma && !single) {
+                            // the earlier visitors' partial sum: one TMA load of the
+                            // fp32 tile into the staging; each thread then adds its
+                            // row and writes it back converted, in place
+                            if (r == 0) {
+                                mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
+                                tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
+                                tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
+                            }
+                            const bool got = wait_group(kBarDq, 128, kDqLoad, ld_it & 1);
+                            ++ld_it;
+                            if (got) {
+                                // 16-bit chunk i (columns 8i..8i+7) from fp32 chunks 2i,
+                                // 2i+1; it lands where fp32 chunk i was, already used
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float4 x0 = *reinterpret_cast<const float4*>(stg + stg_off(r, 2 * i));
+                                    const float4 x1 = *reinterpret_cast<const float4*>(stg + stg_off(r, 2 * i + 1));
+                                    const uint32_t* v = i < 4 ? v0 + 8 * i : v1 + 8 * (i - 4);
+                                    *reinterpret_cast<uint4*>(stg + stg_off(r, i)) = make_uint4(
+                                        pack2<BF16>(fmaf(__uint_as_float(v[0]), a.scale, x0.x),
+                                                    fmaf(__uint_as_float(v[1]), a.scale, x0.y)),
+                                        pack2<BF16>(fmaf(__uint_as_float(v[2]), a.scale, x0.z),
+                                                    fmaf(__uint_as_float(v[3]), a.scale, x0.w)),
+                                        pack2<BF16>(fmaf(__uint_as_float(v[4]), a.scale, x1.x),
+                                                    fmaf(__uint_as_float(v[5]), a.scale, x1.y)),
+                                        pack2<BF16>(fmaf(__uint_as_float(v[6]), a.scale, x1.z),
+                                                    fmaf(__uint_as_float(v[7]), a.scale, x1.w)));
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            named_bar_sync(kBarDq, 128);
+                            if (r == 0 && got) {
+                                tma_put(false, thd, &a.tm_dq, stg_s, 0, th, qrow, tb);
+                                bulk_commit();
+                            }
+                        } else if (conv_now && use_tma) {
                             stage_out(0, v0);
                             stage_out(1, v1);
                             fence_proxy_async_smem();
