@@ -488,9 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         Pending pend{false, false, false, 0, 0, 0u};
         // dV += P^T dO, dK += dS^T Q, dQ = dS K for step `p` (softmax done).
         auto issue_grads = [&](const Pending& p) -> bool {
-            if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
             if (p.first && !wait_warp(kAccEmpty, (acc_it & 1) ^ 1)) return false;
-            ++dq_it;
             const uint32_t sK = sbase + C::kK + p.ks * C::kTile;
             const uint32_t sQ = sbase + C::kQ + p.st * C::kTile, sDO = sbase + C::kDO + p.st * C::kTile;
             const uint32_t sDS = sbase + C::kDS + (p.q_it % C::kDsBufs) * 32768u;
@@ -501,8 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 // K-major (16, 1024) and MN-major (16 KB, 1024) descriptors of the
                 // operand tiles; each contraction step adds its byte offset
                 const uint64_t dDOmn = sdesc_sw128(sDO, kBlock16K, 1024), dQmn = sdesc_sw128(sQ, kBlock16K, 1024);
-                const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024);
-                const uint64_t dDSk = sdesc_sw128(sDS, 16, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
+                const uint64_t dDSk = sdesc_sw128(sDS, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t bdesc = sdesc_at(dDOmn, k * 2048);
@@ -522,13 +519,25 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
                     umma_f16_ss(tm_dk, sdesc_at(dDSk, aoff), sdesc_at(dQmn, k * 2048), kIdPV, acc | (k > 0));
                 }
+                // Q and dO have been read (dQ below reads only dS and K): the
+                // stage goes back to the producer
+                umma_commit(bar(kQEmpty0 + p.st));
+            }
+            __syncwarp();
+            // dQ overwrites the TMEM columns the dQ warps read for the last step;
+            // waiting only here lets dV and dK run meanwhile
+            if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
+            ++dq_it;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ, k > 0);
                 umma_commit(bar(kDqFull));
-                umma_commit(bar(kQEmpty0 + p.st));
                 SWA_TRACE(4, p.q_it);
                 if (p.last) {
+                    // after dQ: the epilogue stages dK/dV in this step's dS^T buffer
                     umma_commit(bar(kAccFull));
                     umma_commit(bar(kKvEmpty0 + p.ks));
                 }
