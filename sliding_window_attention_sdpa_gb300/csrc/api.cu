@@ -13,6 +13,7 @@
 
 #include "../../include/sdpa_bwd.h"
 #include "sdpa_internal.h"
+#include "seq.cuh"
 
 namespace {
 
@@ -266,6 +267,29 @@ sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int d
     return make_map(m, name, base, dt, 2, 64, thd, d, h, rows, b, st);
 }
 
+// The dQ convert kernel zero-fills rows past a sequence's length and q-tiles
+// no kv-tile visits, converts q-tiles whose visitors added with unordered
+// atomics (three or more, not deterministic) and finishes dSink. For a BSHD
+// problem without length arrays every sequence has the same q-tiles, so the
+// launcher can tell on the host that none of this applies and skip the launch.
+bool convert_has_work(const sdpa_bwd_params* p, const swa::Geometry& g)
+{
+    if (p->dsink != nullptr || p->layout != SDPA_BSHD || p->seq_q_lens != nullptr ||
+        p->seq_kv_lens != nullptr)
+        return true;
+    swa::SeqInfo s{};
+    s.slot_q = s.len_q = p->s_q;
+    s.slot_kv = s.len_kv = p->s_kv;
+    s.diag = p->mask_mode == SDPA_MASK_BOTTOM_RIGHT ? p->s_kv - p->s_q : 0;
+    const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
+    for (int64_t j = 0; j < nqt; ++j) {
+        int64_t first, n;
+        swa::q_tile_visitors(g, s, j, first, n);
+        if (n == 0 || (n >= 3 && !p->deterministic)) return true;
+    }
+    return false;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
@@ -396,6 +420,7 @@ sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_
     a.n_row_blocks = w.n_row_blocks;
     a.dsink = p->dsink;
     if (a.n_row_blocks == 0) return SDPA_OK;
+    if (!convert_has_work(p, a.g)) return SDPA_OK;
     return cuda_status(swa::launch_dq_convert(a, p->dtype, static_cast<cudaStream_t>(stream)),
                        "dq_convert launch");
 }

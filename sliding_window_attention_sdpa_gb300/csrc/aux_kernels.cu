@@ -53,8 +53,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 }
 
 // ---------------------------------------------------------------- preprocess
-// grid (ceil(s_q / 128) * 2, h_q, b): 64 rows of one sequence's slot for one
-// q-head, covering every row of every q-tile (rows past the length included).
+// grid (ceil(s_q / 128), h_q, b): one q-tile (kPreRows = 128 rows) of one
+// sequence's slot for one q-head, covering every row of every q-tile (rows
+// past the length included); each thread has four rows' loads in flight.
 // Each row of HD features is read by HD/8 consecutive threads (16 B each).
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
     const bool thd = g.layout == 1;
     float dsink_acc = 0.f;
 
-#pragma unroll 2
+#pragma unroll 4
     for (int r = tid / TPR; r < kPreRows; r += RPP) {
         const int64_t i = i0 + r;
         const bool valid = i < s.len_q;

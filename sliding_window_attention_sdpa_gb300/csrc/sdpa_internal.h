@@ -12,7 +12,7 @@ namespace swa {
 
 constexpr int kTileKV = 128;      // kv rows per CTA work item (MMA M of dK/dV side)
 constexpr int kTileQ = 128;       // q rows per inner-loop step
-constexpr int kPreRows = 64;      // token rows per preprocess CTA
+constexpr int kPreRows = 128;     // token rows per preprocess CTA
 constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;

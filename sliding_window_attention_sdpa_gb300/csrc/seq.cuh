@@ -75,10 +75,10 @@ __device__ __forceinline__ void set_status(int32_t* status, int code)
     atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
-__device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
 
-__device__ __forceinline__ int64_t fdiv(int64_t a, int64_t b)
+__host__ __device__ __forceinline__ int64_t fdiv(int64_t a, int64_t b)
 {
     int64_t q = a / b;
     if ((a % b != 0) && ((a < 0) != (b < 0))) --q;
@@ -88,8 +88,9 @@ __device__ __forceinline__ int64_t fdiv(int64_t a, int64_t b)
 // q-tile range [lo, hi) swept by kv-tile t of a sequence: lo is the first
 // q-tile holding a row that reaches the tile's first key (right bound), hi the
 // clamp ceil((kv_end + W - diag) / tile_q) with kv_end the tile's last key + 1
-// (cuDNN-frontend PR #866, "Change").
-__device__ __forceinline__ void q_tile_range(const Geometry& g, const SeqInfo& s, int64_t t,
+// (cuDNN-frontend PR #866, "Change"). Host-callable: the launcher uses it to
+// tell whether the dQ convert kernel has anything to do.
+__host__ __device__ __forceinline__ void q_tile_range(const Geometry& g, const SeqInfo& s, int64_t t,
                                              int64_t& lo, int64_t& hi)
 {
     const int64_t kv_base = t * kTileKV;
@@ -116,7 +117,7 @@ __device__ __forceinline__ void q_tile_range(const Geometry& g, const SeqInfo& s
 // (both bounds of q_tile_range are non-decreasing in t). `first` is the relay's
 // kv_first = max((q_row0 + diag - W) // tile_kv, 0) (PR #866, "Change"), or 0
 // without a left window.
-__device__ __forceinline__ void q_tile_visitors(const Geometry& g, const SeqInfo& s, int64_t j,
+__host__ __device__ __forceinline__ void q_tile_visitors(const Geometry& g, const SeqInfo& s, int64_t j,
                                                 int64_t& first, int64_t& count)
 {
     const int64_t n_kv = (s.len_kv + kTileKV - 1) / kTileKV;
