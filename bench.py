@@ -119,7 +119,7 @@ class Problem:
         swa._check(swa.sdpa_bwd_gqa_reduce(p, ws, nb, stream), "gqa_reduce")
 
     def launches_per_step(self) -> int:
-        return 3 + (1 if self.h_q != self.h_kv else 0)
+        return self.swa.sdpa_bwd_kernel_launches(self.params)
 
 
 class ClockSampler:

@@ -215,6 +215,16 @@ size_t sdpa_bwd_params_bytes(void);
 int32_t sdpa_bwd_tile_kv(void);
 int32_t sdpa_bwd_tile_q(void);
 
+/*
+ * Number of GPU kernels that sdpa_bwd_preprocess, sdpa_bwd,
+ * sdpa_bwd_dq_convert and sdpa_bwd_gqa_reduce launch, together, for `params`
+ * (sdpa_bwd_no_alloc launches the same ones); -1 if the shape is invalid. No
+ * device work: the counts follow the host-side decisions those calls make
+ * (empty problems launch nothing; dq_convert is skipped when the main kernel
+ * has written every dQ row; gqa_reduce never launches).
+ */
+int32_t sdpa_bwd_kernel_launches(const sdpa_bwd_params *params);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ SDPA_MASK_NONE, SDPA_MASK_TOP_LEFT, SDPA_MASK_BOTTOM_RIGHT = 0, 1, 2
 ENTRY_POINTS = ("sdpa_bwd_workspace_bytes", "sdpa_bwd_preprocess", "sdpa_bwd",
                 "sdpa_bwd_dq_convert", "sdpa_bwd_gqa_reduce", "sdpa_bwd_check_status",
                 "sdpa_bwd_last_error", "sdpa_bwd_params_bytes", "sdpa_bwd_tile_kv",
-                "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc")
+                "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc", "sdpa_bwd_kernel_launches")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -97,6 +97,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.sdpa_bwd_params_bytes.restype = sz
         lib.sdpa_bwd_tile_kv.restype = ctypes.c_int32
         lib.sdpa_bwd_tile_q.restype = ctypes.c_int32
+        lib.sdpa_bwd_kernel_launches.argtypes = [P]
+        lib.sdpa_bwd_kernel_launches.restype = ctypes.c_int32
         _lib = lib
         return lib
 
@@ -121,6 +123,10 @@ def _check(code: int, where: str) -> int:
 
 def sdpa_bwd_workspace_bytes(params: SdpaBwdParams) -> int:
     return int(load().sdpa_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def sdpa_bwd_kernel_launches(params: SdpaBwdParams) -> int:
+    return int(load().sdpa_bwd_kernel_launches(ctypes.byref(params)))
 
 
 def sdpa_bwd_preprocess(params, workspace: int, workspace_bytes: int, stream: int) -> int:

@@ -525,4 +525,21 @@ size_t sdpa_bwd_params_bytes(void) { return sizeof(sdpa_bwd_params); }
 int32_t sdpa_bwd_tile_kv(void) { return swa::kTileKV; }
 int32_t sdpa_bwd_tile_q(void) { return swa::kTileQ; }
 
+int32_t sdpa_bwd_kernel_launches(const sdpa_bwd_params* p)
+{
+    if (check_shape(p) != SDPA_OK) return -1;
+    g_last_error.clear();
+    const swa::WsLayout w = layout_of(p);
+    const int64_t n_kv_tiles = (p->s_kv + swa::kTileKV - 1) / swa::kTileKV;
+    const int64_t stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
+    int32_t n = 0;
+    // the preprocess: a memset instead when there are no rows
+    if (w.n_row_blocks > 0 && stats_row / swa::kPreRows > 0 && p->b > 0 && p->h_q > 0) ++n;
+    // the main kernel: nothing without work items or keys
+    if (p->b * p->h_q * n_kv_tiles != 0 && rows_kv(p) != 0 && p->b * p->h_kv * n_kv_tiles > 0) ++n;
+    // the dQ convert
+    if (w.n_row_blocks > 0 && p->s_q > 0 && p->b > 0 && p->h_q > 0 && convert_has_work(p, geometry_of(p))) ++n;
+    return n;
+}
+
 }  // extern "C"

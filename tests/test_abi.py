@@ -109,3 +109,29 @@ def test_thd_needs_offsets():
     p = base_params(layout=swa.SDPA_THD, total_q=300, total_kv=300)
     assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_INVALID_ARG
     assert "offsets" in swa.last_error()
+
+
+def test_kernel_launch_count():
+    """The four calls launch the preprocess, the main kernel and, when some dQ
+    row is not written by the main kernel (or dSink needs finishing), the
+    convert kernel; gqa_reduce launches nothing."""
+    # top-left causal W=32 over 256 rows: every q-tile has one or two visitors
+    assert swa.sdpa_bwd_kernel_launches(base_params()) == 2
+    # GQA changes nothing
+    assert swa.sdpa_bwd_kernel_launches(base_params(h_kv=2)) == 2
+    # dSink is finished by the convert kernel
+    assert swa.sdpa_bwd_kernel_launches(base_params(sink=4096, dsink=4096)) == 3
+    # with length arrays rows past a sequence's length may need zeros
+    assert swa.sdpa_bwd_kernel_launches(base_params(seq_q_lens=4096)) == 3
+    # no window over 512 rows: q-tile 3 has four visitors, added with atomics
+    # unless deterministic (then the relay's last turn converts)
+    wide = dict(window_left=-1, s_q=512, s_kv=512)
+    assert swa.sdpa_bwd_kernel_launches(base_params(**wide)) == 3
+    assert swa.sdpa_bwd_kernel_launches(base_params(deterministic=1, **wide)) == 2
+    # bottom-right, 128 queries against 512 keys, W=32: q-tile 0 is visited by
+    # kv-tiles 2 and 3 only
+    br = dict(mask_mode=swa.SDPA_MASK_BOTTOM_RIGHT, s_q=128, s_kv=512)
+    assert swa.sdpa_bwd_kernel_launches(base_params(**br)) == 2
+    # no query rows: only the main kernel runs (it writes dK = dV = 0)
+    assert swa.sdpa_bwd_kernel_launches(base_params(s_q=0)) == 1
+    assert swa.sdpa_bwd_kernel_launches(base_params(d=96)) == -1
