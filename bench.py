@@ -182,7 +182,7 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "f606d57dbe14dd8b", "bytes": 249259264},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "8141bdd6348044d5", "bytes": 248453376},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 

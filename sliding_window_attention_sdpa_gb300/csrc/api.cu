@@ -68,11 +68,6 @@ sdpa_status_t check_shape(const sdpa_bwd_params* p)
         if (p->total_q < 0 || p->total_kv < 0)
             return fail(SDPA_ERR_INVALID_ARG, "THD layout: total_q/total_kv must be >= 0");
     }
-    if (p->layout == SDPA_BSHD && p->mask_mode == SDPA_MASK_BOTTOM_RIGHT &&
-        p->seq_q_lens == nullptr && p->seq_kv_lens == nullptr && p->s_q > p->s_kv)
-        return fail(SDPA_ERR_UNSUPPORTED,
-                    "bottom-right causal with s_q=%lld > s_kv=%lld is not supported",
-                    (long long)p->s_q, (long long)p->s_kv);
     if ((p->sink == nullptr) != (p->dsink == nullptr))
         return fail(SDPA_ERR_INVALID_ARG, "sink and dsink must both be set or both be NULL");
     // the main kernel numbers its work items (b x h_kv x kv-tiles) in 32 bits

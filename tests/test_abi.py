@@ -100,9 +100,11 @@ def test_bad_stride_and_workspace():
     assert "need" in swa.last_error()
 
 
-def test_bottom_right_with_longer_queries_is_rejected():
+def test_bottom_right_with_longer_queries_is_accepted():
+    # the first s_q - s_kv rows reach no key; the shape passes validation and
+    # only the (missing) workspace is refused
     p = base_params(mask_mode=swa.SDPA_MASK_BOTTOM_RIGHT, s_q=512)
-    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_UNSUPPORTED
+    assert swa.sdpa_bwd(p, 0, 0, None) == swa.SDPA_ERR_WORKSPACE
 
 
 def test_thd_needs_offsets():

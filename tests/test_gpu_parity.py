@@ -46,6 +46,10 @@ SMALL = [
          thd_lens=[390, 64, 1000], slot_align=8, seed=14),
     Case("br_q_longer_than_kv_lens", 2, 2, 2, 400, 400, 64, "br", 40, lens_q=[400, 300],
          lens_kv=[150, 400], seed=15),
+    # bottom-right with more queries than keys and no length arrays: the first
+    # s_q - s_kv rows reach no key (their LSE is -inf)
+    Case("br_q_longer_than_kv_bshd_gqa4x2", 2, 4, 2, 700, 300, 64, "br", 100, seed=19),
+    Case("br_causal_q_longer_than_kv_bshd_d128", 1, 2, 2, 520, 130, 128, "br", -1, seed=20),
     # window-only with more queries than keys: rows past Lkv + W reach no key
     Case("none_w50_q600_kv300", 1, 2, 2, 600, 300, 64, "none", 50, seed=16),
     # many visitors per q-tile (unordered atomics path) with GQA and a sink

@@ -359,6 +359,23 @@ def test_rows_with_nothing_attended():
     assert np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
 
 
+def test_bottom_right_longer_queries_equals_top_left_on_last_rows():
+    """Bottom-right with Lq > Lkv puts query i at anchor i - (Lq - Lkv): the
+    last Lkv rows are top-left causal on an Lkv x Lkv problem (same window),
+    and the first Lq - Lkv rows reach no key, so they leave dK and dV alone."""
+    br = Problem(b=1, h_q=2, h_kv=1, s_q=11, s_kv=5, d=4, scale=0.5,
+                 mask_mode=MASK_BOTTOM_RIGHT, window_left=2)
+    tl = Problem(**{**br.__dict__, "mask_mode": MASK_TOP_LEFT, "s_q": 5})
+    q, k, v, do, _ = data(br, 19)
+    o, lse, dq, dk, dv, _, _ = full_backward(br, q, k, v, do, None)
+    o2, lse2, dq2, dk2, dv2, _, _ = full_backward(tl, q[:, 6:], k, v, do[:, 6:], None)
+    np.testing.assert_array_equal(o[:, 6:], o2)
+    np.testing.assert_array_equal(dq[:, 6:], dq2)
+    np.testing.assert_array_equal(dk, dk2)
+    np.testing.assert_array_equal(dv, dv2)
+    assert not dq[:, :6].any() and np.all(np.isneginf(lse[:, :, :6]))
+
+
 # ------------------------------------------------ integer identities (tiling)
 
 def _geometries():
