@@ -28,7 +28,8 @@ SDPA_MASK_NONE, SDPA_MASK_TOP_LEFT, SDPA_MASK_BOTTOM_RIGHT = 0, 1, 2
 ENTRY_POINTS = ("sdpa_bwd_workspace_bytes", "sdpa_bwd_preprocess", "sdpa_bwd",
                 "sdpa_bwd_dq_convert", "sdpa_bwd_gqa_reduce", "sdpa_bwd_check_status",
                 "sdpa_bwd_last_error", "sdpa_bwd_params_bytes", "sdpa_bwd_tile_kv",
-                "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc", "sdpa_bwd_kernel_launches")
+                "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc", "sdpa_bwd_kernel_launches",
+                "sdpa_fwd", "sdpa_fwd_check_status", "sdpa_fwd_params_bytes")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -54,6 +55,24 @@ class SdpaBwdParams(ctypes.Structure):
         ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3),
         ("o_stride", _i64x3), ("do_stride", _i64x3),
         ("dq_stride", _i64x3), ("dk_stride", _i64x3), ("dv_stride", _i64x3),
+    ]
+
+
+class SdpaFwdParams(ctypes.Structure):
+    """Mirror of ``sdpa_fwd_params`` (field order and types as in the header)."""
+    _fields_ = [
+        ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32),
+        ("mask_mode", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("b", ctypes.c_int64), ("h_q", ctypes.c_int64), ("h_kv", ctypes.c_int64),
+        ("s_q", ctypes.c_int64), ("s_kv", ctypes.c_int64),
+        ("total_q", ctypes.c_int64), ("total_kv", ctypes.c_int64), ("d", ctypes.c_int64),
+        ("window_left", ctypes.c_int64), ("window_right", ctypes.c_int64),
+        ("scale", ctypes.c_float), ("reserved1", ctypes.c_int32),
+        ("seq_q_lens", ctypes.c_void_p), ("seq_kv_lens", ctypes.c_void_p),
+        ("q_offsets", ctypes.c_void_p), ("kv_offsets", ctypes.c_void_p),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("sink", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3), ("o_stride", _i64x3),
     ]
 
 
@@ -99,6 +118,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.sdpa_bwd_tile_q.restype = ctypes.c_int32
         lib.sdpa_bwd_kernel_launches.argtypes = [P]
         lib.sdpa_bwd_kernel_launches.restype = ctypes.c_int32
+        lib.sdpa_fwd.argtypes = [ctypes.POINTER(SdpaFwdParams), vp]
+        lib.sdpa_fwd.restype = st
+        lib.sdpa_fwd_check_status.argtypes = [vp]
+        lib.sdpa_fwd_check_status.restype = st
+        lib.sdpa_fwd_params_bytes.restype = sz
         _lib = lib
         return lib
 
@@ -282,3 +306,78 @@ def backward(q, k, v, o, dout, lse, *, scale: float, mask_mode: int = SDPA_MASK_
                                      torch.cuda.current_stream().cuda_stream),
                "sdpa_bwd_check_status")
     return dq, dk, dv, dsink
+
+
+def sdpa_fwd(params: SdpaFwdParams, stream) -> int:
+    return load().sdpa_fwd(ctypes.byref(params), stream)
+
+
+def sdpa_fwd_check_status(stream) -> int:
+    return load().sdpa_fwd_check_status(stream)
+
+
+def make_fwd_params(q, k, v, o, lse, *, scale: float, mask_mode: int = SDPA_MASK_TOP_LEFT,
+                    window_left: int = -1, window_right: int = -1, seq_q_lens=None,
+                    seq_kv_lens=None, q_offsets=None, kv_offsets=None,
+                    max_seqlen_q: Optional[int] = None, max_seqlen_kv: Optional[int] = None,
+                    sink=None) -> SdpaFwdParams:
+    """Fill an SdpaFwdParams from torch tensors (BSHD if q is 4-D, THD if 3-D)."""
+    import torch
+    thd = q.dim() == 3
+    layout = SDPA_THD if thd else SDPA_BSHD
+    if q.dtype == torch.bfloat16:
+        dtype = SDPA_BF16
+    elif q.dtype == torch.float16:
+        dtype = SDPA_F16
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    p = SdpaFwdParams()
+    p.dtype, p.layout, p.mask_mode = dtype, layout, mask_mode
+    if thd:
+        if q_offsets is None or kv_offsets is None:
+            raise ValueError("THD layout needs q_offsets and kv_offsets")
+        if max_seqlen_q is None or max_seqlen_kv is None:
+            raise ValueError("THD layout needs max_seqlen_q / max_seqlen_kv (longest slot)")
+        p.b = q_offsets.numel() - 1
+        p.total_q, p.total_kv = q.shape[0], k.shape[0]
+        p.h_q, p.h_kv, p.d = q.shape[1], k.shape[1], q.shape[2]
+        p.s_q, p.s_kv = max_seqlen_q, max_seqlen_kv
+    else:
+        p.b, p.s_q, p.h_q, p.d = q.shape
+        p.s_kv, p.h_kv = k.shape[1], k.shape[2]
+    p.window_left, p.window_right = window_left, window_right
+    p.scale = scale
+    p.seq_q_lens, p.seq_kv_lens = _ptr(seq_q_lens), _ptr(seq_kv_lens)
+    p.q_offsets, p.kv_offsets = _ptr(q_offsets), _ptr(kv_offsets)
+    p.q, p.k, p.v, p.sink, p.o, p.lse = map(_ptr, (q, k, v, sink, o, lse))
+    p.q_stride = _i64x3(*_strides(q, layout))
+    p.k_stride = _i64x3(*_strides(k, layout))
+    p.v_stride = _i64x3(*_strides(v, layout))
+    p.o_stride = _i64x3(*_strides(o, layout))
+    return p
+
+
+def forward(q, k, v, *, scale: float, mask_mode: int = SDPA_MASK_TOP_LEFT, window_left: int = -1,
+            window_right: int = -1, seq_q_lens=None, seq_kv_lens=None, q_offsets=None,
+            kv_offsets=None, max_seqlen_q=None, max_seqlen_kv=None, sink=None,
+            check_status: bool = False):
+    """O and LSE of sliding-window SDPA (the inputs `backward` takes).
+
+    Layouts as in `backward`; returns (o, lse) with o like q and lse fp32
+    [b, h_q, s_q] (BSHD) or [h_q, total_q] (THD).
+    """
+    import torch
+    o = torch.empty_like(q)
+    if q.dim() == 3:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    else:
+        lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    p = make_fwd_params(q, k, v, o, lse, scale=scale, mask_mode=mask_mode, window_left=window_left,
+                        window_right=window_right, seq_q_lens=seq_q_lens, seq_kv_lens=seq_kv_lens,
+                        q_offsets=q_offsets, kv_offsets=kv_offsets, max_seqlen_q=max_seqlen_q,
+                        max_seqlen_kv=max_seqlen_kv, sink=sink)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(sdpa_fwd(p, stream), "sdpa_fwd")
+    if check_status:
+        _check(sdpa_fwd_check_status(stream), "sdpa_fwd_check_status")
+    return o, lse

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswa_sdpa_bwd.so")
-SOURCES = ["api.cu", "aux_kernels.cu", "main_kernel.cu"]
+SOURCES = ["api.cu", "aux_kernels.cu", "main_kernel.cu", "fwd_kernel.cu"]
 HEADERS = ["ptx.cuh", "seq.cuh", "sdpa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -35,8 +35,9 @@ def _digest(extra) -> str:
     for name in SOURCES + HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
-    with open(os.path.join(ROOT, "include", "sdpa_bwd.h"), "rb") as f:
-        h.update(f.read())
+    for name in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        with open(os.path.join(ROOT, "include", name), "rb") as f:
+            h.update(f.read())
     h.update(" ".join(_flags(extra)).encode())
     return h.hexdigest()
 

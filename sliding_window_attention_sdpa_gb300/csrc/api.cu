@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/sdpa_bwd.h"
+#include "../../include/sdpa_fwd.h"
 #include "sdpa_internal.h"
 #include "seq.cuh"
 
@@ -536,5 +537,161 @@ int32_t sdpa_bwd_kernel_launches(const sdpa_bwd_params* p)
     if (w.n_row_blocks > 0 && p->s_q > 0 && p->b > 0 && p->h_q > 0 && convert_has_work(p, geometry_of(p))) ++n;
     return n;
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- forward
+
+namespace {
+
+// The forward's device status word (timeouts), one per device; as for the
+// allocation-free scratch above, host code takes its device address from
+// cudaGetSymbolAddress, once per device.
+static __device__ int32_t g_fwd_status;
+std::mutex g_fwd_mutex;
+int32_t* g_fwd_status_addr[kMaxDevices] = {};
+
+sdpa_status_t fwd_status_word(int32_t** out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDPA_ERR_CUDA, "sdpa_fwd: no current CUDA device (%s)", cudaGetErrorString(e));
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(SDPA_ERR_UNSUPPORTED, "sdpa_fwd: device %d beyond the %d supported", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_fwd_mutex);
+    if (g_fwd_status_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fwd_status);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return fail(SDPA_ERR_CUDA, "sdpa_fwd: cannot resolve the status word on device %d (%s)", dev,
+                        cudaGetErrorString(e));
+        }
+        g_fwd_status_addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_fwd_status_addr[dev];
+    return SDPA_OK;
+}
+
+// The fields the two passes share, in the backward's parameter block, so that
+// the forward uses the same validation and geometry.
+sdpa_bwd_params fwd_view(const sdpa_fwd_params* f)
+{
+    sdpa_bwd_params p{};
+    p.dtype = f->dtype;
+    p.layout = f->layout;
+    p.mask_mode = f->mask_mode;
+    p.deterministic = 0;
+    p.b = f->b;
+    p.h_q = f->h_q;
+    p.h_kv = f->h_kv;
+    p.s_q = f->s_q;
+    p.s_kv = f->s_kv;
+    p.total_q = f->total_q;
+    p.total_kv = f->total_kv;
+    p.d = f->d;
+    p.window_left = f->window_left;
+    p.window_right = f->window_right;
+    p.scale = f->scale;
+    p.seq_q_lens = f->seq_q_lens;
+    p.seq_kv_lens = f->seq_kv_lens;
+    p.q_offsets = f->q_offsets;
+    p.kv_offsets = f->kv_offsets;
+    p.q = f->q;
+    p.k = f->k;
+    p.v = f->v;
+    p.o = f->o;
+    p.lse = f->lse;
+    p.sink = f->sink;
+    p.dsink = const_cast<float*>(f->sink);  // the pairing check has no forward meaning
+    copy3(p.q_stride, f->q_stride);
+    copy3(p.k_stride, f->k_stride);
+    copy3(p.v_stride, f->v_stride);
+    copy3(p.o_stride, f->o_stride);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+sdpa_status_t sdpa_fwd(const sdpa_fwd_params* f, void* stream)
+{
+    if (f == nullptr) return fail(SDPA_ERR_INVALID_ARG, "params is NULL");
+    const sdpa_bwd_params p = fwd_view(f);
+    sdpa_status_t st = check_shape(&p);
+    if (st != SDPA_OK) return st;
+    const bool thd = p.layout == SDPA_THD;
+    const struct { const char* n; const int64_t* s; } strides[] = {
+        {"q", p.q_stride}, {"k", p.k_stride}, {"v", p.v_stride}, {"o", p.o_stride}};
+    for (const auto& x : strides)
+        if ((st = check_strides(x.n, x.s, thd)) != SDPA_OK) return st;
+    const int64_t n_q_tiles = (p.s_q + swa::kTileQ - 1) / swa::kTileQ;
+    if (p.b * p.h_q * n_q_tiles >= (int64_t(1) << 31))
+        return fail(SDPA_ERR_UNSUPPORTED, "%lld forward work items (b x h_q x ceil(s_q/128)): at most 2^31 - 1",
+                    (long long)(p.b * p.h_q * n_q_tiles));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDPA_ERR_CUDA, "no CUDA device available");
+    }
+    const int64_t rq = rows_q(&p), rk = rows_kv(&p);
+    const struct { const char* n; const void* ptr; bool req; } ptrs[] = {
+        {"q", p.q, rq > 0},   {"k", p.k, rk > 0},   {"v", p.v, rk > 0},  {"o", p.o, rq > 0},
+        {"lse", p.lse, rq > 0}, {"sink", p.sink, false}, {"seq_q_lens", p.seq_q_lens, false},
+        {"seq_kv_lens", p.seq_kv_lens, false}, {"q_offsets", p.q_offsets, thd}, {"kv_offsets", p.kv_offsets, thd}};
+    for (const auto& x : ptrs)
+        if ((st = check_device_ptr(x.n, x.ptr, x.req, dev)) != SDPA_OK) return st;
+    if (rq == 0 || p.b == 0) return SDPA_OK;  // no row to write
+    swa::FwdArgs a{};
+    if ((st = fwd_status_word(&a.status)) != SDPA_OK) return st;
+    a.g = geometry_of(&p);
+    a.o = f->o;
+    a.lse = f->lse;
+    a.sink = f->sink;
+    copy3(a.o_stride, f->o_stride);
+    a.n_q_tiles = n_q_tiles;
+    a.scale_log2 = f->scale * 1.4426950408889634f;
+    a.timeout_ns = 2000000000LL;
+    // the maps' row extent is one sequence slot (BSHD: s, where a 4-D map
+    // clips boxes that overhang it) or the packed tokens (THD)
+    const int64_t rq_map = thd ? p.total_q : p.s_q, rk_map = thd ? p.total_kv : p.s_kv;
+    if ((st = make_map(&a.tm_q, "q", p.q, p.dtype, thd, p.d, p.h_q, rq_map, p.b, p.q_stride)) != SDPA_OK ||
+        (st = make_map(&a.tm_o, "o", p.o, p.dtype, thd, p.d, p.h_q, rq_map, p.b, p.o_stride)) != SDPA_OK)
+        return st;
+    if (rk > 0) {
+        if ((st = make_map(&a.tm_k, "k", p.k, p.dtype, thd, p.d, p.h_kv, rk_map, p.b, p.k_stride)) != SDPA_OK ||
+            (st = make_map(&a.tm_v, "v", p.v, p.dtype, thd, p.d, p.h_kv, rk_map, p.b, p.v_stride)) != SDPA_OK)
+            return st;
+    } else {
+        // no keys anywhere: no row admits one and K, V are never loaded
+        a.tm_k = a.tm_q;
+        a.tm_v = a.tm_q;
+    }
+    return cuda_status(swa::launch_fwd(a, p.dtype, static_cast<cudaStream_t>(stream)), "forward launch");
+}
+
+sdpa_status_t sdpa_fwd_check_status(void* stream)
+{
+    int32_t* word = nullptr;
+    sdpa_status_t st = fwd_status_word(&word);
+    if (st != SDPA_OK) return st;
+    if ((st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize")) != SDPA_OK)
+        return st;
+    int32_t host = 0;
+    if ((st = cuda_status(cudaMemcpy(&host, word, sizeof(host), cudaMemcpyDeviceToHost), "status read")) != SDPA_OK)
+        return st;
+    if (host == 0) return SDPA_OK;
+    if ((st = cuda_status(cudaMemset(word, 0, sizeof(int32_t)), "status reset")) != SDPA_OK) return st;
+    if (host == SDPA_ERR_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a forward wait ran out on the device");
+    if (host == SDPA_ERR_UNSUPPORTED)
+        return fail(SDPA_ERR_UNSUPPORTED, "the device gave the forward kernel shared memory not 1024-byte aligned");
+    return fail(SDPA_ERR_CUDA, "unknown forward device status %d", host);
+}
+
+size_t sdpa_fwd_params_bytes(void) { return sizeof(sdpa_fwd_params); }
 
 }  // extern "C"

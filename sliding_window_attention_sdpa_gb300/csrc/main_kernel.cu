@@ -197,18 +197,6 @@ __device__ __forceinline__ void tma_put(bool add, bool thd, const CUtensorMap* m
     }
 }
 
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// The copies committed so far have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
-// The copies committed so far are complete (their global writes performed).
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Orders the async proxy's global writes (completed bulk copies) before the
-// generic-proxy operations that follow, such as a release that publishes them.
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 // Byte offset of 16-byte chunk c of row r in a staged tile of 128-byte rows:
 // blocks of 128 rows x 128 B (8 chunks), chunk c & 7 at position (c & 7) ^ (r % 8)
 // -- the layout a TMA 128-byte-swizzle box of 128 rows reads from shared memory.

@@ -99,9 +99,26 @@ struct CvtArgs {
     float* dsink;
 };
 
+// The forward pass (O and LSE): one work item per (q-tile, q-head, sequence).
+struct FwdArgs {
+    // TMA descriptors of Q, K, V (loads) and O (stores): 64 x 1 x 128 boxes,
+    // 128-byte swizzle; BSHD 4-D (d, h, s, b), THD 3-D (d, h, t).
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    Geometry g;
+    void* o;                  // O (I/O dtype)
+    float* lse;               // LSE, natural log, fp32 (backward's layout)
+    const float* sink;        // [h_q] or null
+    int64_t o_stride[3];
+    int64_t n_q_tiles;        // q-tiles per sequence slot
+    float scale_log2;         // scale * log2(e)
+    int32_t* status;          // device status word (timeouts)
+    int64_t timeout_ns;
+};
+
 // Launchers (defined next to their kernels). Return the launch error.
 cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_main(const MainArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_fwd(const FwdArgs& a, int dtype, cudaStream_t s);
 
 }  // namespace swa

@@ -65,6 +65,8 @@ class Built:
     checks: list    # (label, selector(outputs) -> tensor, expected numpy) triples
     dsink_heads: Optional[np.ndarray]
     dsink_want: Optional[np.ndarray]
+    ref_o: Optional[np.ndarray] = None    # oracle forward (fp64), whole-problem builds
+    ref_lse: Optional[np.ndarray] = None
 
 
 def _f64(x):
@@ -91,6 +93,7 @@ def build(case: Case, device="cuda", units=None) -> Built:
     sink_np = None if t.sink is None else _f64(t.sink)
     checks = []
     dsink_heads, dsink_want = None, None
+    ref_o, ref_lse = None, None
 
     def problem(**kw):
         base = dict(d=case.d, scale=case.scale, mask_mode=MODES[case.mask],
@@ -110,6 +113,7 @@ def build(case: Case, device="cuda", units=None) -> Built:
                            seq_kv_lens=None if case.lens_kv is None else np.asarray(case.lens_kv, np.int32))
         q, k, v, do = _f64(t.q), _f64(t.k), _f64(t.v), _f64(t.do)
         o, lse = oracle.forward(prob, q, k, v, sink_np)
+        ref_o, ref_lse = o, lse
         o_io = torch.from_numpy(o).to(io)
         lse32 = torch.from_numpy(lse).float()
         dq, dk, dv, _, dsink = oracle.backward(prob, q, k, v, _f64(o_io), do,
@@ -187,7 +191,7 @@ def build(case: Case, device="cuda", units=None) -> Built:
             kw["seq_q_lens"] = torch.tensor(case.lens_q, dtype=torch.int32, device=device)
         if case.lens_kv is not None:
             kw["seq_kv_lens"] = torch.tensor(case.lens_kv, dtype=torch.int32, device=device)
-    return Built(case, dev, kw, checks, dsink_heads, dsink_want)
+    return Built(case, dev, kw, checks, dsink_heads, dsink_want, ref_o, ref_lse)
 
 
 def run_gpu(bt: Built, **over):
