@@ -102,6 +102,14 @@ class Problem:
                                       self.dk, self.dv, scale=self.scale, mask_mode=MODE[mask],
                                       window_left=w, deterministic=deterministic)
         self.ws = swa.alloc_workspace(self.params, device)
+        # the forward on the same inputs (its own outputs)
+        self.fo = torch.empty_like(self.q)
+        self.flse = torch.empty_like(self.lse)
+        self.fparams = swa.make_fwd_params(self.q, self.k, self.v, self.fo, self.flse, scale=self.scale,
+                                           mask_mode=MODE[mask], window_left=w)
+        self.fwd_flops = 4 * d * attended_pairs(sq, skv, mask, w) * b * hq
+        # Q, K, V read once, O and LSE written once
+        self.fwd_bytes = b * sq * hq * (2 * 2 * d + 4) + b * skv * hkv * 2 * 2 * d
         self.flops = 10 * d * attended_pairs(sq, skv, mask, w) * b * hq
         self.main_bytes = algorithmic_bytes(b, hq, hkv, sq, skv, d, hq != hkv)
 
@@ -182,24 +190,29 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "8141bdd6348044d5", "bytes": 248453376},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "20aabdfb6bdb86ba", "bytes": 248363520},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
+# The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
+FWD_TRAFFIC = {
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "2982e2f3b4117490", "bytes": 114745088},
+}
+FWD_SOURCES = ("fwd_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 
 
-def main_kernel_digest() -> str:
+def main_kernel_digest(sources=KERNEL_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sliding_window_attention_sdpa_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(name: str):
-    t = MAIN_TRAFFIC.get(name)
-    if t is None or t["kernel"] != main_kernel_digest():
+def measured_traffic(name: str, table=MAIN_TRAFFIC, sources=KERNEL_SOURCES):
+    t = table.get(name)
+    if t is None or t["kernel"] != main_kernel_digest(sources):
         return None
     return t["bytes"]
 
@@ -233,6 +246,24 @@ def time_device(prob: Problem, steps: int, warmup: int):
     total = [a.elapsed_time(d) for a, _, _, d in ev]
     main = [b.elapsed_time(c) for _, b, c, _ in ev]
     return total, main
+
+
+def time_forward(prob: Problem, steps: int, warmup: int):
+    """Per-call device time (ms) of the forward, L2 flushed before each call."""
+    swa = prob.swa
+    sid = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=prob.q.device)
+    for _ in range(warmup):
+        swa._check(swa.sdpa_fwd(prob.fparams, sid), "sdpa_fwd")
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush.fill_(1.0)
+        a.record()
+        swa._check(swa.sdpa_fwd(prob.fparams, sid), "sdpa_fwd")
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int):
@@ -401,7 +432,10 @@ def main():
         total, main_ms = time_device(prob, args.steps, args.warmup)
         torch.cuda.synchronize()
         e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps // 2), 2)
+        fwd_ms = time_forward(prob, args.steps, args.warmup)
     step_ms = sum(total) / len(total)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    fwd_status = swa.sdpa_fwd_check_status(torch.cuda.current_stream().cuda_stream)
     main_avg = sum(main_ms) / len(main_ms)
     status = swa.sdpa_bwd_check_status(prob.ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
@@ -434,6 +468,14 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": prob.launches_per_step() * args.steps,
         "clocks": clk.summary(),
+        # the forward (O, LSE) on the same workload, timed after the backward's
+        # region; 4 d FLOPs per attended pair and head
+        "forward": {"ms": fwd_avg, "tflops": prob.fwd_flops / (fwd_avg * 1e-3) / 1e12,
+                    "kernel": "sdpa_fwd_kernel", "algorithmic_bytes": prob.fwd_bytes,
+                    "hbm_frac": prob.fwd_bytes / (fwd_avg * 1e-3) / 1e9 / peak_gbs,
+                    "tensor_peak_frac": prob.fwd_flops / (fwd_avg * 1e-3) / 1e12 / peak_tf,
+                    "traffic": measured_traffic(args.workload, FWD_TRAFFIC, FWD_SOURCES),
+                    "device_status": int(fwd_status)},
     }
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1

@@ -137,3 +137,46 @@ def test_kernel_launch_count():
     # no query rows: only the main kernel runs (it writes dK = dV = 0)
     assert swa.sdpa_bwd_kernel_launches(base_params(s_q=0)) == 1
     assert swa.sdpa_bwd_kernel_launches(base_params(d=96)) == -1
+
+
+def test_forward_params_struct_matches_binding(lib):
+    assert lib.sdpa_fwd_params_bytes() == ctypes.sizeof(swa.SdpaFwdParams)
+
+
+def fwd_params(**kw):
+    p = swa.SdpaFwdParams()
+    p.dtype, p.layout, p.mask_mode = swa.SDPA_BF16, swa.SDPA_BSHD, swa.SDPA_MASK_TOP_LEFT
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 2, 4, 4, 256, 256, 64
+    p.window_left, p.window_right, p.scale = 32, -1, 0.125
+    st = swa._i64x3(256 * 4 * 64, 4 * 64, 64)
+    for f in ("q", "k", "v", "o"):
+        setattr(p, f + "_stride", st)
+        setattr(p, f, 4096)
+    p.lse = 4096
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,code,needle", [
+    ("dtype", 7, swa.SDPA_ERR_INVALID_ARG, "dtype"),
+    ("layout", 3, swa.SDPA_ERR_INVALID_ARG, "layout"),
+    ("mask_mode", 9, swa.SDPA_ERR_INVALID_ARG, "mask_mode"),
+    ("h_kv", 3, swa.SDPA_ERR_INVALID_ARG, "multiple of h_kv"),
+    ("d", 80, swa.SDPA_ERR_UNSUPPORTED, "d=80"),
+    ("window_right", -7, swa.SDPA_ERR_INVALID_ARG, "window_right"),
+    ("scale", 0.0, swa.SDPA_ERR_INVALID_ARG, "scale"),
+])
+def test_forward_host_validation(field, value, code, needle):
+    assert swa.sdpa_fwd(fwd_params(**{field: value}), None) == code
+    assert needle in swa.last_error()
+
+
+def test_forward_bad_stride_and_thd_offsets():
+    p = fwd_params()
+    p.o_stride = swa._i64x3(256 * 4 * 64, 4 * 64 + 3, 64)
+    assert swa.sdpa_fwd(p, None) == swa.SDPA_ERR_INVALID_ARG
+    assert "o_stride[1]" in swa.last_error()
+    p = fwd_params(layout=swa.SDPA_THD, total_q=300, total_kv=300)
+    assert swa.sdpa_fwd(p, None) == swa.SDPA_ERR_INVALID_ARG
+    assert "offsets" in swa.last_error()
