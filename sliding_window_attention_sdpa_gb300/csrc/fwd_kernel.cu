@@ -11,9 +11,10 @@
 //
 // Warp roles (256 threads):
 //   warp 0      TMA producer: Q per item; K, V per kv-tile into a 2-stage ring
-//   warp 1      MMA issuer (one thread) and TMEM owner; S of kv-tile t + 1 is
-//               issued before P V of kv-tile t, so the softmax of one kv-tile
-//               overlaps the tensor core's work on the next
+//   warp 1      MMA issuer (lane 0 of the converged warp) and TMEM owner;
+//               S of kv-tile t + 1 is issued before P V of kv-tile t, so the
+//               softmax of one kv-tile overlaps the tensor core's work on the
+//               next
 //   warps 2-3   idle
 //   warps 4-7   softmax and epilogue, one q row (TMEM lane) per thread, the
 //               whole 128-column S row in registers: m' = max(m, max_j s_j),
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kFThreads, 1) sdpa_fwd_kernel(const __grid_con
                 if (!wait_warp(fOEmpty, (o_it & 1) ^ 1)) return false;
                 ++o_it;
             }
-            if (lane == 0) {
+            {
                 tc_fence_after();
                 const uint64_t dP = sdesc_sw128(sbase + C::kP, 16, 1024);
                 const uint64_t dV = sdesc_sw128(sbase + C::kV + pd.st * C::kTile, kFBlock, 1024);
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kFThreads, 1) sdpa_fwd_kernel(const __grid_con
                     fzero_tail<HD>(sm + C::kV + st * C::kTile, it.s.len_kv - t * kTileKV, lane);
                 const int sb = s_it & 1;
                 if (!(ok = wait_warp(fSFree0 + sb, ((s_it >> 1) & 1) ^ 1))) break;
-                if (lane == 0) {
+                {
                     tc_fence_after();
                     const uint64_t dQ = sdesc_sw128(sbase + C::kQ, 16, 1024);
                     const uint64_t dK = sdesc_sw128(sbase + C::kK + st * C::kTile, 16, 1024);

@@ -20,10 +20,10 @@
 //   warp 0      TMA producer: K, V per item; Q, dO per q-tile into a ring of
 //               kStages stages (128-byte swizzle, zero fill past the tensor),
 //               each with the q-tile's per-row (LSE log2, D) pairs (1 KB bulk copy)
-//   warp 1      MMA issuer (one thread) and TMEM owner. At d = 64 it issues the
-//               next q-tile's S^T/dP^T ahead of this q-tile's dV/dK/dQ, so the
-//               softmax of one q-tile overlaps the gradient contractions of the
-//               previous one (dS^T double-buffered)
+//   warp 1      MMA issuer (lane 0 of the converged warp) and TMEM owner. At
+//               d = 64 it issues the next q-tile's S^T/dP^T ahead of this
+//               q-tile's dV/dK/dQ, so the softmax of one q-tile overlaps the
+//               gradient contractions of the previous one (dS^T double-buffered)
 //   warps 2-3   idle
 //   warps 4-11  softmax: two warps per TMEM sub-partition, each thread one kv
 //               row (TMEM lane) and one 64-column half of the q-tile; recomputes
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             const uint32_t sK = sbase + C::kK + p.ks * C::kTile;
             const uint32_t sQ = sbase + C::kQ + p.st * C::kTile, sDO = sbase + C::kDO + p.st * C::kTile;
             const uint32_t sDS = sbase + C::kDS + (p.q_it % C::kDsBufs) * 32768u;
-            if (lane == 0) {
+            {
                 SWA_TRACE(3, p.q_it);
                 tc_fence_after();
                 const uint32_t acc = p.first ? 0u : 1u;
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             // waiting only here lets dV and dK run meanwhile
             if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
             ++dq_it;
-            if (lane == 0) {
+            {
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
 #pragma unroll
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 // S^T and dP^T overwrite TMEM that the previous dQ may alias
                 if (C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
                 const uint32_t sQ = sbase + C::kQ + st * C::kTile, sDO = sbase + C::kDO + st * C::kTile;
-                if (lane == 0) {
+                {
                     tc_fence_after();
                     const uint64_t dK = sdesc_sw128(sK, 16, 1024), dQ = sdesc_sw128(sQ, 16, 1024);
                     const uint64_t dV = sdesc_sw128(sV, 16, 1024), dDO = sdesc_sw128(sDO, 16, 1024);
