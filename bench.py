@@ -5,8 +5,11 @@ d=64, S=8192, top-left causal with a 128-key left window, bf16, non-deterministi
 dQ (the configuration the cuDNN-frontend pages time on A100 at 0.980 ms).
 
 A step is one whole backward: preprocess, main, dq_convert, gqa_reduce (a
-no-op for MHA) -- every kernel of the path. The L2 cache is flushed (a 512 MB
-write) between timed steps, outside the per-step CUDA events.
+no-op for MHA) -- every kernel of the path. The L2 cache is flushed between
+timed steps, outside the per-step CUDA events: a 512 MB write, then a 512 MB
+read of another buffer, so that none of the step's data is cached and no
+dirty line of the flush is left for the step's first kernel to write back
+(the cold, clean state in which ncu times kernels).
 
   value      attended TFLOP/s (10*d FLOPs per attended (q, k) pair per head)
              with inputs resident in HBM, summed over ranks / max-over-ranks time
@@ -53,6 +56,20 @@ WORKLOADS = {
 DEFAULT = "gptoss_b2_h16_d64_w128_s8192"
 MODE = {"none": 0, "tl": 1, "br": 2}
 L2_FLUSH_BYTES = 512 << 20
+
+
+class L2Flush:
+    """Evicts everything from the 129 MB L2: writes one buffer larger than it,
+    then reads another (the read evicts the written lines, which are written
+    back here rather than inside the next timed region)."""
+
+    def __init__(self, device):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        self.r.sum()
 
 
 def attended_pairs(s_q: int, s_kv: int, mask: str, w: int) -> int:
@@ -230,7 +247,7 @@ def time_device(prob: Problem, steps: int, warmup: int):
     """Per-step device time (ms) of the whole backward and of the main kernel."""
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=prob.q.device)
+    flush = L2Flush(prob.q.device)
     for _ in range(warmup):
         prob.step(sid)
     torch.cuda.synchronize()
@@ -238,7 +255,7 @@ def time_device(prob: Problem, steps: int, warmup: int):
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for e in ev:
-        flush.fill_(1.0)
+        flush()
         e[0].record()
         prob.step(sid, (e[1], e[2]))
         e[3].record()
@@ -252,13 +269,13 @@ def time_forward(prob: Problem, steps: int, warmup: int):
     """Per-call device time (ms) of the forward, L2 flushed before each call."""
     swa = prob.swa
     sid = torch.cuda.current_stream().cuda_stream
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=prob.q.device)
+    flush = L2Flush(prob.q.device)
     for _ in range(warmup):
         swa._check(swa.sdpa_fwd(prob.fparams, sid), "sdpa_fwd")
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
-        flush.fill_(1.0)
+        flush()
         a.record()
         swa._check(swa.sdpa_fwd(prob.fparams, sid), "sdpa_fwd")
         b.record()
@@ -373,7 +390,7 @@ def workload_config(name):
             "heads_kv": hkv, "head_dim": d, "mask": {"tl": "top_left_causal",
                                                      "br": "bottom_right_causal",
                                                      "none": "window_only"}[mask],
-            "window_left": w, "l2": "flushed (512 MB write) between timed steps",
+            "window_left": w, "l2": "flushed between timed steps (512 MB write, then 512 MB read of another buffer)",
             "parallelism": "replicas"}
 
 

@@ -126,8 +126,9 @@ size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params *params);
  * formula): D[b,h,i] = sum_d dO*O in fp32 for every row; zeroes the per-q-tile
  * relay counters, the status word and (non-deterministic mode) the fp32 dQ
  * accumulator rows of q-tiles that three or more kv-tiles visit; writes the
- * dSink partials -exp(sink_h - LSE_i) * D_i summed over each block of 128
- * unpadded rows.
+ * dSink partials -exp(sink_h - LSE_i) * D_i summed over each block of
+ * unpadded rows. O and dO are read by TMA in blocks of up to 16 q-heads x 16
+ * rows (d = 64; 8 rows at d = 128; more rows with fewer heads).
  */
 sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params *params, void *workspace,
                                   size_t workspace_bytes, void *stream);

@@ -122,7 +122,7 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     const int64_t rq = rows_q(p);
     const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
     w.n_sems = p->b * p->h_q * nqt;
-    w.n_row_blocks = p->b * ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * (swa::kTileQ / swa::kPreRows);
+    w.n_row_blocks = p->b * ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * (swa::kTileQ / swa::pre_tile(p->h_q, p->d).rows);
     size_t off = 0;
     w.status = off;
     off = align256(off + 16);
@@ -254,6 +254,33 @@ sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, CUten
     return SDPA_OK;
 }
 
+// Descriptor of a 16-bit tensor read in whole-row boxes of d x box_h heads x
+// box_rows rows, unswizzled (the preprocess's O and dO).
+sdpa_status_t make_box_map(CUtensorMap* m, const char* name, const void* base, int dtype, bool thd, int64_t d,
+                           int64_t h, int64_t rows, int64_t b, const int64_t* st, uint32_t box_h, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const CUtensorMapDataType dt =
+        dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int64_t esize = 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                          static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(b)};
+    cuuint64_t hs = h > 1 ? static_cast<cuuint64_t>(st[2] * esize) : static_cast<cuuint64_t>(d * esize);
+    cuuint64_t ss = rows > 1 ? static_cast<cuuint64_t>(st[1] * esize) : hs * h;
+    cuuint64_t bs = b > 1 ? static_cast<cuuint64_t>(st[0] * esize) : ss * (rows > 0 ? rows : 1);
+    cuuint64_t strides[3] = {hs, ss, bs};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), box_h, box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, dt, thd ? 3 : 4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SDPA_ERR_UNSUPPORTED, "%s: TMA descriptor rejected (error %d) for strides (%lld, %lld, %lld)",
+                    name, (int)r, (long long)st[0], (long long)st[1], (long long)st[2]);
+    return SDPA_OK;
+}
+
 // Descriptor of a 16-bit I/O tensor (64-element boxes).
 sdpa_status_t make_map(CUtensorMap* m, const char* name, const void* base, int dtype, bool thd,
                        int64_t d, int64_t h, int64_t rows, int64_t b, const int64_t* st)
@@ -332,6 +359,16 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
             st = cuda_status(cudaMemsetAsync(p->dsink, 0, p->h_q * sizeof(float), s), "dsink memset");
         return st;
     }
+    const swa::PreTile pt = swa::pre_tile(p->h_q, p->d);
+    a.pre_heads = pt.heads;
+    a.pre_rows = pt.rows;
+    const bool thd = p->layout == SDPA_THD;
+    const int64_t rq = thd ? p->total_q : p->s_q;
+    if ((st = make_box_map(&a.tm_o, "o", p->o, p->dtype, thd, p->d, p->h_q, rq, p->b, p->o_stride, pt.heads,
+                           pt.rows)) != SDPA_OK ||
+        (st = make_box_map(&a.tm_do, "dout", p->dout, p->dtype, thd, p->d, p->h_q, rq, p->b, p->do_stride, pt.heads,
+                           pt.rows)) != SDPA_OK)
+        return st;
     return cuda_status(swa::launch_preprocess(a, p->dtype, s), "preprocess launch");
 }
 
@@ -530,7 +567,7 @@ int32_t sdpa_bwd_kernel_launches(const sdpa_bwd_params* p)
     const int64_t stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
     int32_t n = 0;
     // the preprocess: a memset instead when there are no rows
-    if (w.n_row_blocks > 0 && stats_row / swa::kPreRows > 0 && p->b > 0 && p->h_q > 0) ++n;
+    if (w.n_row_blocks > 0 && stats_row > 0 && p->b > 0 && p->h_q > 0) ++n;
     // the main kernel: nothing without work items or keys
     if (p->b * p->h_q * n_kv_tiles != 0 && rows_kv(p) != 0 && p->b * p->h_kv * n_kv_tiles > 0) ++n;
     // the dQ convert

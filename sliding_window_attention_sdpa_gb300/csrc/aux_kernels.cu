@@ -53,99 +53,171 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 }
 
 // ---------------------------------------------------------------- preprocess
-// grid (ceil(s_q / 128), h_q, b): one q-tile (kPreRows = 128 rows) of one
-// sequence's slot for one q-head, covering every row of every q-tile (rows
-// past the length included); each thread has four rows' loads in flight.
-// Each row of HD features is read by HD/8 consecutive threads (16 B each).
-template <int HD, bool BF16>
-__global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a)
+// Persistent CTAs (one per SM) walk blocks of pre_rows token rows x pre_heads
+// q-heads (block = (sequence, row block, head chunk), head chunk fastest). The
+// TMA engine stages each block's O and dO boxes in a 3-stage shared-memory
+// ring; each thread then reduces one (row, head) unit of HD features (d = 64)
+// or half of one (d = 128) from shared memory. The per-element work of the
+// register path (address arithmetic per 16 bytes, cross-thread reductions)
+// made it issue-bound at about half the HBM bandwidth. Every row of every
+// q-tile is covered: rows past the length get the statistics that make P = 0.
+constexpr int kPreStages = 3;
+constexpr uint32_t kPreBox = 32768;   // bytes of one tensor's box: 256 threads x 128 B
+
+__device__ __forceinline__ void pre_tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool thd,
+                                             int head, int row, int batch)
 {
-    constexpr int TPR = HD / 8;          // threads per row
-    constexpr int RPP = 256 / TPR;       // rows per pass
+    if (thd)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(head), "r"(row)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(head), "r"(row), "r"(batch)
+            : "memory");
+}
+
+template <int HD, bool BF16>
+__global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constant__ PreArgs a)
+{
+    constexpr int TPU = HD / 64;   // threads per (row, head) unit, 128 B each
+    extern __shared__ __align__(1024) uint8_t smem[];
+    // [stage][O box | dO box], dSink row terms [2][256] fp32, mbarriers
+    float* red = reinterpret_cast<float*>(smem + kPreStages * 2 * kPreBox);
+    const uint32_t sbase = smem_u32(smem);
+    if (sbase & 127u) {   // TMA destinations need 128-byte alignment
+        if (threadIdx.x == 0) set_status(a.status, kStatusUnsupported);
+        return;
+    }
+    const uint32_t bars = sbase + kPreStages * 2 * kPreBox + 2 * 256 * 4;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
-    const int c = tid % TPR;
-    const int64_t h = blockIdx.y, bi = blockIdx.z;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kPreRows;
+    const bool thd = g.layout == 1;
     const bool with_sink = a.sink != nullptr;
+    const int hc_n = a.pre_heads, rows_n = a.pre_rows;
+    const int units = hc_n * rows_n;
+    const uint32_t box_bytes = static_cast<uint32_t>(units) * HD * 2;
+    const int64_t nrb = a.stats_row / rows_n;              // row blocks per sequence
+    const int64_t nhc = (g.h_q + hc_n - 1) / hc_n;         // head chunks
+    const int64_t n_items = g.b * nrb * nhc;
 
     // relay / visit counters, ticket and status: zeroed by the whole grid
     {
-        const int64_t nthr = static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z * blockDim.x;
-        const int64_t id = ((static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x +
-                            blockIdx.x) * blockDim.x + tid;
+        const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
         for (int64_t k = id; k < a.n_sems; k += nthr) a.sems[k] = 0;
         if (id == 0) {
             a.status[0] = 0;
             a.status[1] = 0;
         }
     }
-    const SeqInfo s = seq_info(g, bi);
-    const int64_t blk = bi * gridDim.x + blockIdx.x;  // dSink partial slot
-    const float sink = with_sink ? a.sink[h] : 0.f;
-    // q-tiles with three or more visitors take unordered atomics (unless
-    // deterministic): their accumulator rows start at zero
-    bool zero_acc = false;
-    if (!a.deterministic && i0 < s.len_q) {
-        int64_t first, n;
-        q_tile_visitors(g, s, i0 / kTileQ, first, n);
-        zero_acc = n >= 3;
+    if (tid == 0) {
+        for (int st = 0; st < kPreStages; ++st) mbar_init(bars + 8u * st, 1);
+        fence_mbar_init();
     }
-    const uint16_t* o = static_cast<const uint16_t*>(a.o);
-    const uint16_t* dout = static_cast<const uint16_t*>(a.dout);
-    const bool thd = g.layout == 1;
-    float dsink_acc = 0.f;
+    __syncthreads();
 
-#pragma unroll 4
-    for (int r = tid / TPR; r < kPreRows; r += RPP) {
-        const int64_t i = i0 + r;
-        const bool valid = i < s.len_q;
+    struct Blk {
+        int64_t bi, rb, hc;
+    };
+    auto coords = [&](int64_t item) -> Blk {
+        const int64_t rest = item / nhc;
+        return Blk{rest / nrb, rest % nrb, item % nhc};
+    };
+    // thread 0: stage the O and dO boxes of `item` into ring entry `st`
+    auto issue = [&](int64_t item, int st) {
+        const Blk b = coords(item);
+        const int64_t row0 = thd ? g.q_offsets[b.bi] : 0;
+        const int row = static_cast<int>(row0 + b.rb * rows_n);
+        const uint32_t bar = bars + 8u * st;
+        mbar_arrive_expect_tx(bar, 2 * box_bytes);
+        const uint32_t dst = sbase + st * 2 * kPreBox;
+        pre_tma_load(dst, &a.tm_o, bar, thd, static_cast<int>(b.hc * hc_n), row, static_cast<int>(b.bi));
+        pre_tma_load(dst + kPreBox, &a.tm_do, bar, thd, static_cast<int>(b.hc * hc_n), row, static_cast<int>(b.bi));
+    };
+    if (tid == 0)
+        for (int st = 0; st < kPreStages; ++st) {
+            const int64_t item = blockIdx.x + static_cast<int64_t>(st) * gridDim.x;
+            if (item < n_items) issue(item, st);
+        }
+
+    const int u = tid / TPU, half = tid % TPU;
+    const int r = u / hc_n, hl = u - r * hc_n;   // this thread's unit in every block
+    const bool in_box = u < units;
+    int j = 0;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+        const int st = j % kPreStages;
+        const Blk b = coords(item);
+        const SeqInfo s = seq_info(g, b.bi);
+        const int64_t h = b.hc * hc_n + hl;
+        const int64_t i = b.rb * rows_n + r;
+        const bool unit = in_box && h < g.h_q;       // a (row, head) of the slot's row space
+        const bool valid = unit && i < s.len_q;
+        // the row's LSE, loaded before the wait for the box
+        float lse = -INFINITY;
+        if (valid && half == 0)
+            lse = __ldg(a.lse + (thd ? h * g.rows_q + s.q_row0 + i : (b.bi * g.h_q + h) * g.s_q + i));
+        // q-tiles with three or more visitors take unordered atomics (unless
+        // deterministic): their accumulator rows start at zero
+        bool zero_acc = false;
+        if (!a.deterministic && b.rb * rows_n < s.len_q) {
+            int64_t first, n;
+            q_tile_visitors(g, s, (b.rb * rows_n) / kTileQ, first, n);
+            zero_acc = n >= 3;
+        }
+        const bool got = __syncthreads_and(mbar_wait(bars + 8u * st, (j / kPreStages) & 1, 2000000000ull));
+        if (!got) {
+            if (tid == 0) set_status(a.status, kStatusTimeout);
+            return;
+        }
         float part = 0.f;
-        if (valid) {
-            const int64_t oo = (thd ? (s.q_row0 + i) * a.o_stride[1] : bi * a.o_stride[0] + i * a.o_stride[1]) +
-                               h * a.o_stride[2] + c * 8;
-            const int64_t od = (thd ? (s.q_row0 + i) * a.do_stride[1] : bi * a.do_stride[0] + i * a.do_stride[1]) +
-                               h * a.do_stride[2] + c * 8;
-            float fo[8], fd[8];
-            unpack8<BF16>(ld_nc_v4(o + oo), fo);
-            unpack8<BF16>(ld_nc_v4(dout + od), fd);
+        if (in_box) {
+            const uint8_t* po = smem + st * 2 * kPreBox + u * (HD * 2) + half * 128;
+            const uint8_t* pd = po + kPreBox;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) part = fmaf(fo[e], fd[e], part);
+            for (int k = 0; k < 8; ++k) {
+                // rotated chunk order: the 8 threads sharing a 128-byte line
+                // read different banks
+                const int c = (k + tid) & 7;
+                float fo[8], fd[8];
+                unpack8<BF16>(*reinterpret_cast<const uint4*>(po + c * 16), fo);
+                unpack8<BF16>(*reinterpret_cast<const uint4*>(pd + c * 16), fd);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part = fmaf(fo[e], fd[e], part);
+            }
         }
+        if constexpr (TPU == 2) part += __shfl_xor_sync(0xffffffffu, part, 1);
         if (zero_acc && valid) {
-            float4* z = reinterpret_cast<float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8);
-            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            float4* z = reinterpret_cast<float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + half * 64);
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (c == 0) {
+            for (int k = 0; k < 16; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (unit && half == 0) {
             // per-row statistics for the main kernel, one slot for every row of
             // every q-tile: (LSE * log2(e), D); rows past the length or that
             // attend nothing get (+inf, 0) so that P = 0 there
-            float l2 = INFINITY;
-            if (valid) {
-                const int64_t so = thd ? h * g.rows_q + s.q_row0 + i : (bi * g.h_q + h) * g.s_q + i;
-                const float lse = a.lse[so];
-                if (lse != -INFINITY) {
-                    l2 = lse * 1.4426950408889634f;
-                    if (with_sink) dsink_acc -= expf(sink - lse) * part;
-                }
+            float l2 = INFINITY, ds = 0.f;
+            if (valid && lse != -INFINITY) {
+                l2 = lse * 1.4426950408889634f;
+                if (with_sink) ds = -expf(a.sink[h] - lse) * part;
             }
-            a.stats[(bi * g.h_q + h) * a.stats_row + i] = make_float2(l2, valid ? part : 0.f);
+            a.stats[(b.bi * g.h_q + h) * a.stats_row + i] = make_float2(l2, valid ? part : 0.f);
+            if (with_sink) red[(j & 1) * 256 + hl * rows_n + r] = ds;
         }
-    }
-
-    if (with_sink) {
-        __shared__ float red[8];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dsink_acc += __shfl_xor_sync(0xffffffffu, dsink_acc, off);
-        if ((tid & 31) == 0) red[tid >> 5] = dsink_acc;
-        __syncthreads();
+        __syncthreads();   // ring entry st is read; dSink terms are written
         if (tid == 0) {
+            const int64_t next = item + static_cast<int64_t>(kPreStages) * gridDim.x;
+            if (next < n_items) issue(next, st);
+        }
+        if (with_sink && tid < hc_n && b.hc * hc_n + tid < g.h_q) {
+            // this block's dSink partial of a head: its rows summed in order
             float t = 0.f;
-            for (int w = 0; w < 8; ++w) t += red[w];
-            a.dsink_part[h * a.n_row_blocks + blk] = t;
+            for (int k = 0; k < rows_n; ++k) t += red[(j & 1) * 256 + tid * rows_n + k];
+            a.dsink_part[(b.hc * hc_n + tid) * a.n_row_blocks + b.bi * nrb + b.rb] = t;
         }
     }
 }
@@ -165,11 +237,15 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
     const int c = tid % TPR;
     const int64_t j = blockIdx.x, h = blockIdx.y, bi = blockIdx.z;
     if (a.dsink != nullptr && j == 0 && h == 0 && bi == 0) {
-        // fixed-order finish: bitwise repeatable
-        for (int64_t hh = tid; hh < g.h_q; hh += blockDim.x) {
+        // fixed-order finish, a warp per head: lane l sums partials l, l + 32,
+        // ... in order, then a fixed butterfly; bitwise repeatable
+        const int lane = tid & 31;
+        for (int64_t hh = tid >> 5; hh < g.h_q; hh += blockDim.x >> 5) {
             float t = 0.f;
-            for (int64_t k = 0; k < a.n_row_blocks; ++k) t += a.dsink_part[hh * a.n_row_blocks + k];
-            a.dsink[hh] = t;
+            for (int64_t k = lane; k < a.n_row_blocks; k += 32) t += a.dsink_part[hh * a.n_row_blocks + k];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+            if (lane == 0) a.dsink[hh] = t;
         }
     }
     const SeqInfo s = seq_info(g, bi);
@@ -220,10 +296,26 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
 
 cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
 {
-    const int64_t nx = a.stats_row / kPreRows;  // every row of every q-tile
-    if (nx == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(nx), static_cast<unsigned>(a.g.h_q), static_cast<unsigned>(a.g.b));
-    SWA_DISPATCH(preprocess_kernel, a, grid, s);
+    if (a.stats_row == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
+    const int64_t items = a.g.b * (a.stats_row / a.pre_rows) * ((a.g.h_q + a.pre_heads - 1) / a.pre_heads);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+    const size_t smem = kPreStages * 2 * kPreBox + 2 * 256 * 4 + 8 * kPreStages;
+#define SWA_PRE(HD, BF)                                                                                   \
+    do {                                                                                                  \
+        if ((e = cudaFuncSetAttribute(preprocess_kernel<HD, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                      static_cast<int>(smem))) != cudaSuccess)                            \
+            return e;                                                                                     \
+        preprocess_kernel<HD, BF><<<grid, 256, smem, s>>>(a);                                             \
+    } while (0)
+    if (a.g.d == 64 && dtype == 0) SWA_PRE(64, true);
+    else if (a.g.d == 64) SWA_PRE(64, false);
+    else if (dtype == 0) SWA_PRE(128, true);
+    else SWA_PRE(128, false);
+#undef SWA_PRE
     return cudaGetLastError();
 }
 

@@ -852,11 +852,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             const Item it = decode(a, cnt, item);
             if (!it.has_work) continue;
             for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, it.advance(j, hh)) {
-                if (r == 0) bulk_wait_read0();   // the staging is free again
-                if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
-                if (r == 0) SWA_TRACE(9, dq_it);
-                ++dq_it;
-                tc_fence_after();
+                // this visit's bookkeeping first, while the dQ contraction runs
+                // (after the wait it delayed the TMEM read by ~1 K cycles)
                 int64_t first, nvis;
                 q_tile_visitors(g, it.s, j, first, nvis);
                 const int turn = static_cast<int>(it.t - first);
@@ -864,7 +861,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
                 // two visitors, or deterministic mode: hand the tile along in turn order
                 const bool relay = a.deterministic || nvis == 2;
-                const bool accumulate = !single && !relay;
                 const bool conv_now = single || (relay && turn == nvis - 1);
                 // accumulator write: a store for the first relay turn, else an add
                 const bool add = !(relay && turn == 0);
@@ -873,6 +869,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const bool use_tma = !thd || (j + 1) * kTileQ <= it.s.slot_q;
                 const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
                 const int tb = static_cast<int>(it.bi), th = static_cast<int>(hh);
+                if (r == 0) bulk_wait_read0();   // the staging is free again
+                if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
+                if (r == 0) SWA_TRACE(9, dq_it);
+                ++dq_it;
+                tc_fence_after();
                 // Waits for this visit's turn (relay) in thread 0; true in all 128
                 // threads if the turn came (or none was needed) and nothing aborted.
                 auto wait_turn = [&]() -> bool {

@@ -12,7 +12,20 @@ namespace swa {
 
 constexpr int kTileKV = 128;      // kv rows per CTA work item (MMA M of dK/dV side)
 constexpr int kTileQ = 128;       // q rows per inner-loop step
-constexpr int kPreRows = 128;     // token rows per preprocess CTA
+// Preprocess block: up to 16 q-heads x `rows` token rows, the most that one
+// 256-thread CTA covers with one (row, head) unit (d = 64) or half a unit
+// (d = 128) per thread; rows is a power of two that divides 128.
+struct PreTile {
+    int heads, rows;
+};
+inline __host__ __device__ PreTile pre_tile(int64_t h_q, int64_t d)
+{
+    const int heads = h_q < 16 ? static_cast<int>(h_q) : 16;
+    const int units = 256 / static_cast<int>(d / 64);
+    int rows = 1;
+    while (rows * 2 * heads <= units && rows < 128) rows *= 2;
+    return PreTile{heads, rows};
+}
 constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;
@@ -44,6 +57,10 @@ struct Geometry {
 };
 
 struct PreArgs {
+    // TMA descriptors of O and dO (BSHD 4-D (d, h, s, b), THD 3-D (d, h, t)),
+    // boxes of d x pre_heads x pre_rows, no swizzle
+    CUtensorMap tm_o, tm_do;
+    int32_t pre_heads, pre_rows;
     Geometry g;
     const void* o;
     const void* dout;
