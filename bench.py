@@ -207,12 +207,12 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "20aabdfb6bdb86ba", "bytes": 248363520},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "17edf0fa50583237", "bytes": 248302848},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
 FWD_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "2982e2f3b4117490", "bytes": 114745088},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "890d65db1bcee198", "bytes": 114843136},
 }
 FWD_SOURCES = ("fwd_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 
