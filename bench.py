@@ -15,7 +15,8 @@ dirty line of the flush is left for the step's first kernel to write back
              with inputs resident in HBM, summed over ranks / max-over-ranks time
   e2e        the same metric through the public API from pinned host buffers,
              host->device copies of Q, K, V, O, dO, LSE and the device->host
-             read of dQ, dK, dV inside every timed step
+             read of dQ, dK, dV inside every timed step (consecutive steps'
+             copies and compute overlap on three streams)
   roofline   the main kernel: algorithmic bytes per launch / its mean duration
              (CUDA events on the launching stream) against measured HBM peak
   cpu_baseline  the fp64 CPU oracle on the same workload (host cores)
@@ -284,31 +285,56 @@ def time_forward(prob: Problem, steps: int, warmup: int):
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int):
-    """Same backward through the public API from pinned host buffers."""
+    """Same backward through the public API from pinned host buffers.
+
+    Every step copies its inputs (Q, K, V, O, dO, LSE) host -> device, runs
+    `backward()` and copies dQ, dK, dV device -> host, all inside the timed
+    region. The three stages of consecutive steps overlap on three streams,
+    as a training loop would feed its batches: the copy of step k + 1's inputs
+    and the read of step k - 1's results run while step k computes. Device
+    input buffers alternate between two sets. Returns (ms per step, host ->
+    device bytes per step, device -> host bytes per step).
+    """
     import sliding_window_attention_sdpa_gb300 as swa
-    host_in = [t.cpu().pin_memory() for t in (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)]
+    names = (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)
+    host_in = [t.cpu().pin_memory() for t in names]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (prob.dq, prob.dk, prob.dv)]
-    dev_in = [torch.empty_like(t) for t in (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)]
+    dev_in = [[torch.empty_like(t) for t in names] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     kw = dict(scale=prob.scale, mask_mode=MODE[prob.mask], window_left=prob.w,
               workspace=prob.ws)
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    for e in done:
+        e.record(s_run)
 
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        dq, dk, dv, _ = swa.backward(*dev_in, **kw)
-        for h, d in zip(host_out, (dq, dk, dv)):
-            h.copy_(d, non_blocking=True)
+    def one(k):
+        buf = k % 2
+        s_in.wait_event(done[buf])           # step k - 2 has read this input set
+        with torch.cuda.stream(s_in):
+            for d, h in zip(dev_in[buf], host_in):
+                d.copy_(h, non_blocking=True)
+        copied[buf].record(s_in)
+        s_run.wait_event(copied[buf])
+        with torch.cuda.stream(s_run):
+            dq, dk, dv, _ = swa.backward(*dev_in[buf], **kw)
+        done[buf].record(s_run)
+        s_out.wait_event(done[buf])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(host_out, (dq, dk, dv)):
+                d.record_stream(s_out)
+                h.copy_(d, non_blocking=True)
 
-    for _ in range(warmup):
-        one()
+    for k in range(warmup):
+        one(k)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a.record(s_in)
+    for k in range(steps):
+        one(warmup + k)
+    b.record(s_out)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps, h2d, d2h
 
@@ -448,7 +474,7 @@ def main():
     with ClockSampler(local) as clk:
         total, main_ms = time_device(prob, args.steps, args.warmup)
         torch.cuda.synchronize()
-        e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps // 2), 2)
+        e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps), 2)
         fwd_ms = time_forward(prob, args.steps, args.warmup)
     step_ms = sum(total) / len(total)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
@@ -482,7 +508,9 @@ def main():
                      "kernel": "sdpa_bwd_main_kernel", "peak_kind": peak_kind,
                      "algorithmic_bytes": prob.main_bytes},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_max,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "step k+1's host->device copy and step k-1's device->host read run "
+                           "during step k (three streams)"},
         "gpu_launches": prob.launches_per_step() * args.steps,
         "clocks": clk.summary(),
         # the forward (O, LSE) on the same workload, timed after the backward's
