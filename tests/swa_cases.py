@@ -16,7 +16,7 @@ other units get filler inputs (O = 0, LSE = 10) and are not compared.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 from typing import List, Optional
 
 import numpy as np
@@ -67,6 +67,8 @@ class Built:
     dsink_want: Optional[np.ndarray]
     ref_o: Optional[np.ndarray] = None    # oracle forward (fp64), whole-problem builds
     ref_lse: Optional[np.ndarray] = None
+    # sampled builds: (label, o selector, expected o, lse selector, expected lse)
+    fwd_checks: list = field(default_factory=list)
 
 
 def _f64(x):
@@ -92,6 +94,7 @@ def build(case: Case, device="cuda", units=None) -> Built:
                             device=case.gen_device)
     sink_np = None if t.sink is None else _f64(t.sink)
     checks = []
+    fwd_checks = []
     dsink_heads, dsink_want = None, None
     ref_o, ref_lse = None, None
 
@@ -157,6 +160,8 @@ def build(case: Case, device="cuda", units=None) -> Built:
             if thd:
                 o_dev[rows, hs] = o_io[0].to(device)
                 lse_dev[hs, rows] = lse32[0].to(device)
+                fwd_checks.append((f"[{bi},{g}]", lambda o_, r=rows, h=hs: o_[r, h], o[0],
+                                   lambda l_, r=rows, h=hs: l_[h, r], lse[0]))
                 checks += [
                     (f"dq[{bi},{g}]", lambda out, r=rows, h=hs: out[0][r, h], dq[0]),
                     (f"dk[{bi},{g}]", lambda out, r=rows, h=gs: out[1][r, h], dk[0]),
@@ -164,6 +169,8 @@ def build(case: Case, device="cuda", units=None) -> Built:
             else:
                 o_dev[bi, :, hs] = o_io[0].to(device)
                 lse_dev[bi, hs] = lse32[0].to(device)
+                fwd_checks.append((f"[{bi},{g}]", lambda o_, b_=bi, h=hs: o_[b_, :, h], o[0],
+                                   lambda l_, b_=bi, h=hs: l_[b_, h], lse[0]))
                 checks += [
                     (f"dq[{bi},{g}]", lambda out, b_=bi, h=hs: out[0][b_, :, h], dq[0]),
                     (f"dk[{bi},{g}]", lambda out, b_=bi, h=gs: out[1][b_, :, h], dk[0]),
@@ -191,7 +198,7 @@ def build(case: Case, device="cuda", units=None) -> Built:
             kw["seq_q_lens"] = torch.tensor(case.lens_q, dtype=torch.int32, device=device)
         if case.lens_kv is not None:
             kw["seq_kv_lens"] = torch.tensor(case.lens_kv, dtype=torch.int32, device=device)
-    return Built(case, dev, kw, checks, dsink_heads, dsink_want, ref_o, ref_lse)
+    return Built(case, dev, kw, checks, dsink_heads, dsink_want, ref_o, ref_lse, fwd_checks)
 
 
 def run_gpu(bt: Built, **over):

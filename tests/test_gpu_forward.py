@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from swa_cases import Case, build, compare
-from test_gpu_parity import SMALL
+from test_gpu_parity import FULL, SMALL
 
 pytestmark = pytest.mark.gpu
 
@@ -70,3 +70,31 @@ def test_forward_is_repeatable():
     o1, l1 = run_forward(bt)
     o2, l2 = run_forward(bt)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# the forward has no deterministic mode: one case per input set
+FWD_FULL = [(c, u) for c, u in FULL if not c.det]
+
+
+@pytest.mark.parametrize("case,units", FWD_FULL, ids=lambda x: x.name if isinstance(x, Case) else "")
+def test_forward_full_size_sampled(case, units):
+    """The benchmark's full-size workloads in the launch configuration the
+    benchmark times (every CTA walks several items per slot): the forward of
+    the whole problem, compared on the oracle's sampled (sequence, kv-head)
+    units."""
+    import sliding_window_attention_sdpa_gb300 as swa
+    bt = build(case, units=units)
+    d, kw = bt.dev, dict(bt.kwargs)
+    kw.pop("deterministic", None)
+    o, lse = swa.forward(d["q"], d["k"], d["v"], check_status=True, **kw)
+    torch.cuda.synchronize()
+    assert bt.fwd_checks
+    for label, osel, o_want, lsel, l_want in bt.fwd_checks:
+        compare(f"{case.name} o{label}", osel(o), o_want, case.dtype)
+        got = lsel(lse).double().cpu().numpy()
+        inf_w, inf_g = np.isneginf(l_want), np.isneginf(got)
+        assert np.array_equal(inf_w, inf_g), f"{case.name} lse{label}: -inf rows differ"
+        err = np.abs(got[~inf_w] - l_want[~inf_w])
+        assert err.size == 0 or err.max() <= 2e-3, f"{case.name} lse{label}: max error {err.max():.3e}"
+    del bt, o, lse
+    torch.cuda.empty_cache()
