@@ -61,8 +61,8 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 // register path (address arithmetic per 16 bytes, cross-thread reductions)
 // made it issue-bound at about half the HBM bandwidth. Every row of every
 // q-tile is covered: rows past the length get the statistics that make P = 0.
-constexpr int kPreStages = 3;
-constexpr uint32_t kPreBox = 32768;   // bytes of one tensor's box: 256 threads x 128 B
+constexpr uint32_t kPreRing = 196608;   // bytes of the ring: stages of an O box and a dO box
+constexpr int kPreMaxStages = 8;
 
 __device__ __forceinline__ void pre_tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool thd,
                                              int head, int row, int batch)
@@ -87,13 +87,13 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
     constexpr int TPU = HD / 64;   // threads per (row, head) unit, 128 B each
     extern __shared__ __align__(1024) uint8_t smem[];
     // [stage][O box | dO box], dSink row terms [2][256] fp32, mbarriers
-    float* red = reinterpret_cast<float*>(smem + kPreStages * 2 * kPreBox);
+    float* red = reinterpret_cast<float*>(smem + kPreRing);
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 127u) {   // TMA destinations need 128-byte alignment
         if (threadIdx.x == 0) set_status(a.status, kStatusUnsupported);
         return;
     }
-    const uint32_t bars = sbase + kPreStages * 2 * kPreBox + 2 * 256 * 4;
+    const uint32_t bars = sbase + kPreRing + 2 * 256 * 4;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
     const bool thd = g.layout == 1;
@@ -101,9 +101,13 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
     const int hc_n = a.pre_heads, rows_n = a.pre_rows;
     const int units = hc_n * rows_n;
     const uint32_t box_bytes = static_cast<uint32_t>(units) * HD * 2;
-    const int64_t nrb = a.stats_row / rows_n;              // row blocks per sequence
-    const int64_t nhc = (g.h_q + hc_n - 1) / hc_n;         // head chunks
-    const int64_t n_items = g.b * nrb * nhc;
+    // block counts fit 32 bits (the host checks): no 64-bit divisions here
+    const uint32_t nrb = static_cast<uint32_t>(a.stats_row / rows_n);   // row blocks per sequence
+    const uint32_t nhc = static_cast<uint32_t>((g.h_q + hc_n - 1) / hc_n);   // head chunks
+    const uint32_t n_items = static_cast<uint32_t>(g.b) * nrb * nhc;
+    // as many ring stages as boxes of this size fit
+    const uint32_t stage_bytes = 2 * box_bytes;
+    const int n_stages = static_cast<int>(min(kPreRing / stage_bytes, static_cast<uint32_t>(kPreMaxStages)));
 
     // relay / visit counters, ticket and status: zeroed by the whole grid
     {
@@ -116,32 +120,32 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
         }
     }
     if (tid == 0) {
-        for (int st = 0; st < kPreStages; ++st) mbar_init(bars + 8u * st, 1);
+        for (int st = 0; st < n_stages; ++st) mbar_init(bars + 8u * st, 1);
         fence_mbar_init();
     }
     __syncthreads();
 
     struct Blk {
-        int64_t bi, rb, hc;
+        uint32_t bi, rb, hc;
     };
-    auto coords = [&](int64_t item) -> Blk {
-        const int64_t rest = item / nhc;
-        return Blk{rest / nrb, rest % nrb, item % nhc};
+    auto coords = [&](uint32_t item) -> Blk {
+        const uint32_t rest = item / nhc;
+        return Blk{rest / nrb, rest % nrb, item - rest * nhc};
     };
     // thread 0: stage the O and dO boxes of `item` into ring entry `st`
-    auto issue = [&](int64_t item, int st) {
+    auto issue = [&](uint32_t item, int st) {
         const Blk b = coords(item);
         const int64_t row0 = thd ? g.q_offsets[b.bi] : 0;
         const int row = static_cast<int>(row0 + b.rb * rows_n);
         const uint32_t bar = bars + 8u * st;
         mbar_arrive_expect_tx(bar, 2 * box_bytes);
-        const uint32_t dst = sbase + st * 2 * kPreBox;
+        const uint32_t dst = sbase + st * stage_bytes;
         pre_tma_load(dst, &a.tm_o, bar, thd, static_cast<int>(b.hc * hc_n), row, static_cast<int>(b.bi));
-        pre_tma_load(dst + kPreBox, &a.tm_do, bar, thd, static_cast<int>(b.hc * hc_n), row, static_cast<int>(b.bi));
+        pre_tma_load(dst + box_bytes, &a.tm_do, bar, thd, static_cast<int>(b.hc * hc_n), row, static_cast<int>(b.bi));
     };
     if (tid == 0)
-        for (int st = 0; st < kPreStages; ++st) {
-            const int64_t item = blockIdx.x + static_cast<int64_t>(st) * gridDim.x;
+        for (int st = 0; st < n_stages; ++st) {
+            const uint32_t item = blockIdx.x + st * gridDim.x;
             if (item < n_items) issue(item, st);
         }
 
@@ -149,12 +153,13 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
     const int r = u / hc_n, hl = u - r * hc_n;   // this thread's unit in every block
     const bool in_box = u < units;
     int j = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
-        const int st = j % kPreStages;
+    int st = 0;
+    uint32_t phase = 0;
+    for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
         const Blk b = coords(item);
         const SeqInfo s = seq_info(g, b.bi);
-        const int64_t h = b.hc * hc_n + hl;
-        const int64_t i = b.rb * rows_n + r;
+        const int64_t h = static_cast<int64_t>(b.hc) * hc_n + hl;
+        const int64_t i = static_cast<int64_t>(b.rb) * rows_n + r;
         const bool unit = in_box && h < g.h_q;       // a (row, head) of the slot's row space
         const bool valid = unit && i < s.len_q;
         // the row's LSE, loaded before the wait for the box
@@ -169,15 +174,15 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
             q_tile_visitors(g, s, (b.rb * rows_n) / kTileQ, first, n);
             zero_acc = n >= 3;
         }
-        const bool got = __syncthreads_and(mbar_wait(bars + 8u * st, (j / kPreStages) & 1, 2000000000ull));
+        const bool got = __syncthreads_and(mbar_wait(bars + 8u * st, phase, 2000000000ull));
         if (!got) {
             if (tid == 0) set_status(a.status, kStatusTimeout);
             return;
         }
         float part = 0.f;
         if (in_box) {
-            const uint8_t* po = smem + st * 2 * kPreBox + u * (HD * 2) + half * 128;
-            const uint8_t* pd = po + kPreBox;
+            const uint8_t* po = smem + st * stage_bytes + u * (HD * 2) + half * 128;
+            const uint8_t* pd = po + box_bytes;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 // rotated chunk order: the 8 threads sharing a 128-byte line
@@ -210,14 +215,18 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
         }
         __syncthreads();   // ring entry st is read; dSink terms are written
         if (tid == 0) {
-            const int64_t next = item + static_cast<int64_t>(kPreStages) * gridDim.x;
+            const uint32_t next = item + n_stages * gridDim.x;
             if (next < n_items) issue(next, st);
         }
         if (with_sink && tid < hc_n && b.hc * hc_n + tid < g.h_q) {
             // this block's dSink partial of a head: its rows summed in order
             float t = 0.f;
             for (int k = 0; k < rows_n; ++k) t += red[(j & 1) * 256 + tid * rows_n + k];
-            a.dsink_part[(b.hc * hc_n + tid) * a.n_row_blocks + b.bi * nrb + b.rb] = t;
+            a.dsink_part[(b.hc * hc_n + tid) * a.n_row_blocks + static_cast<int64_t>(b.bi) * nrb + b.rb] = t;
+        }
+        if (++st == n_stages) {
+            st = 0;
+            phase ^= 1u;
         }
     }
 }
@@ -298,12 +307,13 @@ cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
 {
     if (a.stats_row == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
     const int64_t items = a.g.b * (a.stats_row / a.pre_rows) * ((a.g.h_q + a.pre_heads - 1) / a.pre_heads);
+    if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // blocks are counted in 32 bits
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-    const size_t smem = kPreStages * 2 * kPreBox + 2 * 256 * 4 + 8 * kPreStages;
+    const size_t smem = kPreRing + 2 * 256 * 4 + 8 * kPreMaxStages;
 #define SWA_PRE(HD, BF)                                                                                   \
     do {                                                                                                  \
         if ((e = cudaFuncSetAttribute(preprocess_kernel<HD, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
