@@ -91,8 +91,12 @@ typedef struct sdpa_bwd_params {
     int32_t dtype;          /* SDPA_BF16 | SDPA_F16 for Q, K, V, O, dO, dQ, dK, dV */
     int32_t layout;         /* SDPA_BSHD | SDPA_THD */
     int32_t mask_mode;      /* SDPA_MASK_* */
-    int32_t deterministic;  /* 0: dQ by unordered fp32 atomics; 1: ordered relay,
-                               bitwise repeatable results */
+    int32_t deterministic;  /* 0: dQ by unordered fp32 atomics; 1: bitwise
+                               repeatable: per-visitor partial slots summed in
+                               visitor order where a q-tile can have three or
+                               more visitors and the slots fit 2 GiB of
+                               workspace, else the ordered relay; 2: bitwise
+                               repeatable, ordered relay only */
     int64_t b;              /* batch size (THD: number of sequences) */
     int64_t h_q, h_kv;      /* heads; h_q % h_kv == 0 (MHA, GQA, MQA) */
     int64_t s_q, s_kv;      /* BSHD: padded lengths; THD: longest slot */
@@ -116,8 +120,10 @@ typedef struct sdpa_bwd_params {
 /*
  * Workspace size in bytes for `params` (0 on invalid params; see
  * sdpa_bwd_last_error). The workspace holds the fp32 dQ accumulator, D = rowsum
- * (dO*O), the relay counters, the dSink partials and the status word. It must be 256-byte
- * aligned device memory; its contents need no initialisation.
+ * (dO*O), the relay counters, the dSink partials, the status word and, in
+ * deterministic mode 1 when a q-tile can have three or more visitors, up to
+ * 2 GiB of per-visitor partial dQ tiles. It must be 256-byte aligned device
+ * memory; its contents need no initialisation.
  */
 size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params *params);
 
@@ -141,19 +147,23 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params *params, void *workspace
  * group sum (PR #557) happens in place, in head order; stores dK, dV.
  * dQ = scale * dS K of a q-tile is combined over the contiguous kv-tiles that
  * visit it, [kv_first, kv_first + n) with kv_first = max((q_row0 + diag - W)
- * // tile_kv, 0): a lone visitor stores dQ directly; in deterministic mode,
- * or with two visitors, the tile passes along the relay (turn t - kv_first)
- * through the fp32 accumulator and the last turn stores dQ; otherwise the
- * visitors add with fp32 atomics and sdpa_bwd_dq_convert stores dQ.
+ * // tile_kv, 0): a lone visitor stores dQ directly; with two visitors, or in
+ * deterministic mode without slots, the tile passes along the relay (turn
+ * t - kv_first) through the fp32 accumulator and the last turn stores dQ; in
+ * deterministic mode with slots (three or more visitors), each visitor stores
+ * its fp32 partial in its own slot (turn) and sdpa_bwd_dq_convert sums them in
+ * visitor order; otherwise the visitors add with fp32 atomics and
+ * sdpa_bwd_dq_convert stores dQ.
  */
 sdpa_status_t sdpa_bwd(const sdpa_bwd_params *params, void *workspace, size_t workspace_bytes,
                        void *stream);
 
 /*
  * dQ convert ("cvt" kernel): dQ = dtype(fp32 accumulator) on the q-tiles that
- * took unordered atomics, dQ = 0 on rows no kv-tile visits (padding, gap
- * tokens, rows outside every window), and dsink[h] = fixed-order sum of the
- * dSink partials (when a sink is used).
+ * took unordered atomics, dQ = dtype(sum of the visitors' partial slots, in
+ * visitor order) on the q-tiles that used slots, dQ = 0 on rows no kv-tile
+ * visits (padding, gap tokens, rows outside every window), and dsink[h] =
+ * fixed-order sum of the dSink partials (when a sink is used).
  */
 sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params *params, void *workspace,
                                   size_t workspace_bytes, void *stream);

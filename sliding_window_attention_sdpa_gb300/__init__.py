@@ -207,7 +207,7 @@ def _strides(t, layout: int):
 
 def make_params(q, k, v, o, dout, lse, dq, dk, dv, *, scale: float,
                 mask_mode: int = SDPA_MASK_TOP_LEFT, window_left: int = -1,
-                window_right: int = -1, deterministic: bool = False,
+                window_right: int = -1, deterministic: int = 0,
                 seq_q_lens=None, seq_kv_lens=None, q_offsets=None, kv_offsets=None,
                 max_seqlen_q: Optional[int] = None, max_seqlen_kv: Optional[int] = None,
                 sink=None, dsink=None) -> SdpaBwdParams:
@@ -223,7 +223,9 @@ def make_params(q, k, v, o, dout, lse, dq, dk, dv, *, scale: float,
         raise ValueError(f"unsupported dtype {q.dtype}")
     p = SdpaBwdParams()
     p.dtype, p.layout, p.mask_mode = dtype, layout, mask_mode
-    p.deterministic = 1 if deterministic else 0
+    # False/0: unordered atomics; True/1: bitwise repeatable (per-visitor
+    # slots where they apply, else the relay); 2: bitwise repeatable, relay only
+    p.deterministic = int(deterministic) if deterministic in (0, 1, 2) else 1
     if thd:
         if q_offsets is None or kv_offsets is None:
             raise ValueError("THD layout needs q_offsets and kv_offsets")
@@ -277,7 +279,7 @@ def alloc_workspace(params: SdpaBwdParams, device):
 
 
 def backward(q, k, v, o, dout, lse, *, scale: float, mask_mode: int = SDPA_MASK_TOP_LEFT,
-             window_left: int = -1, window_right: int = -1, deterministic: bool = False,
+             window_left: int = -1, window_right: int = -1, deterministic: int = 0,
              seq_q_lens=None, seq_kv_lens=None, q_offsets=None, kv_offsets=None,
              max_seqlen_q=None, max_seqlen_kv=None, sink=None, workspace=None,
              check_status: bool = False):

@@ -45,8 +45,8 @@ sdpa_status_t check_shape(const sdpa_bwd_params* p)
         return fail(SDPA_ERR_INVALID_ARG, "layout: expected SDPA_BSHD or SDPA_THD, got %d", p->layout);
     if (p->mask_mode < SDPA_MASK_NONE || p->mask_mode > SDPA_MASK_BOTTOM_RIGHT)
         return fail(SDPA_ERR_INVALID_ARG, "mask_mode: unknown value %d", p->mask_mode);
-    if (p->deterministic != 0 && p->deterministic != 1)
-        return fail(SDPA_ERR_INVALID_ARG, "deterministic: expected 0 or 1, got %d", p->deterministic);
+    if (p->deterministic < 0 || p->deterministic > 2)
+        return fail(SDPA_ERR_INVALID_ARG, "deterministic: expected 0, 1 or 2, got %d", p->deterministic);
     if (p->b < 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s_q < 0 || p->s_kv < 0)
         return fail(SDPA_ERR_INVALID_ARG,
                     "shape: b=%lld h_q=%lld h_kv=%lld s_q=%lld s_kv=%lld (need b,s >= 0, h > 0)",
@@ -116,6 +116,24 @@ sdpa_status_t check_device_ptr(const char* name, const void* ptr, bool required,
 int64_t rows_q(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_q : p->b * p->s_q; }
 int64_t rows_kv(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_kv : p->b * p->s_kv; }
 
+// Largest number of kv-tiles that can visit one q-tile: the keys a q-tile's
+// rows attend span tile_q + W_left + W_right positions (plus one tile for the
+// alignment); all kv-tiles when the window is unbounded on either side.
+int64_t visitor_bound(const sdpa_bwd_params* p)
+{
+    const int64_t nkv = (p->s_kv + swa::kTileKV - 1) / swa::kTileKV;
+    const int64_t right = p->mask_mode == SDPA_MASK_NONE ? p->window_right
+                                                          : (p->window_right > 0 ? p->window_right : 0);
+    if (p->window_left < 0 || right < 0) return nkv;
+    const int64_t span = swa::kTileQ + p->window_left + right;
+    const int64_t b = (span + swa::kTileKV - 1) / swa::kTileKV + 1;
+    return b < nkv ? b : nkv;
+}
+
+// Most workspace the per-visitor dQ slots may take; beyond it deterministic
+// mode keeps the relay.
+constexpr size_t kSlotCapBytes = size_t(2) << 30;
+
 swa::WsLayout layout_of(const sdpa_bwd_params* p)
 {
     swa::WsLayout w{};
@@ -134,6 +152,19 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     off = align256(off + static_cast<size_t>(w.n_sems) * 4);
     w.dsink_part = off;
     if (p->sink != nullptr) off = align256(off + static_cast<size_t>(p->h_q) * w.n_row_blocks * 4);
+    // Deterministic mode (1): q-tiles that three or more kv-tiles visit keep one
+    // fp32 partial per visitor, summed in visitor order by the convert kernel,
+    // instead of passing one tile along the relay, when the slots fit the cap.
+    w.dq_part = off;
+    w.n_slots = 0;
+    if (p->deterministic == 1) {
+        const int64_t bound = visitor_bound(p);
+        const size_t bytes = static_cast<size_t>(p->b) * p->h_q * nqt * bound * swa::kTileQ * p->d * 4;
+        if (bound >= 3 && bytes <= kSlotCapBytes) {
+            w.n_slots = bound;
+            off = align256(off + bytes);
+        }
+    }
     w.total = off;
     return w;
 }
@@ -300,6 +331,7 @@ bool convert_has_work(const sdpa_bwd_params* p, const swa::Geometry& g)
     if (p->dsink != nullptr || p->layout != SDPA_BSHD || p->seq_q_lens != nullptr ||
         p->seq_kv_lens != nullptr)
         return true;
+    const bool slots = layout_of(p).n_slots > 0;
     swa::SeqInfo s{};
     s.slot_q = s.len_q = p->s_q;
     s.slot_kv = s.len_kv = p->s_kv;
@@ -308,7 +340,7 @@ bool convert_has_work(const sdpa_bwd_params* p, const swa::Geometry& g)
     for (int64_t j = 0; j < nqt; ++j) {
         int64_t first, n;
         swa::q_tile_visitors(g, s, j, first, n);
-        if (n == 0 || (n >= 3 && !p->deterministic)) return true;
+        if (n == 0 || (n >= 3 && (!p->deterministic || slots))) return true;
     }
     return false;
 }
@@ -435,6 +467,18 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
         a.tm_dq = a.tm_k;
         a.tm_acc = a.tm_k;
     }
+    // per-visitor partial dQ tiles: rows of d fp32 values, one 128-row tile
+    // per (sequence, q-head, q-tile, visitor)
+    a.n_slots = rq > 0 ? w.n_slots : 0;
+    if (a.n_slots > 0) {
+        const int64_t rows = p->b * p->h_q * a.n_q_tiles * a.n_slots * swa::kTileQ;
+        const int64_t part_st[3] = {rows * p->d, p->d, p->d};
+        if ((st = make_map(&a.tm_part, "dq partials", at<float>(ws, w.dq_part), CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           4, 32, true, p->d, 1, rows, 1, part_st)) != SDPA_OK)
+            return st;
+    } else {
+        a.tm_part = a.tm_k;
+    }
     return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
 }
 
@@ -446,6 +490,9 @@ sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_
     swa::CvtArgs a{};
     a.g = geometry_of(p);
     a.dq_acc = at<float>(ws, w.dq_acc);
+    a.dq_part = at<float>(ws, w.dq_part);
+    a.n_slots = w.n_slots;
+    a.n_q_tiles = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
     a.deterministic = p->deterministic;
     a.dq = p->dq;
     copy3(a.dq_stride, p->dq_stride);

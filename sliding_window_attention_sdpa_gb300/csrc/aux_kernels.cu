@@ -4,7 +4,9 @@
 //  * dq_convert ("cvt"): the main kernel already stored dQ (converted by each
 //    q-tile's last visitor); this writes dQ = 0 on the rows no kv-tile visits
 //    (padding, gap tokens, rows outside every window), converts the q-tiles
-//    that took unordered atomics, and finishes dSink.
+//    that took unordered atomics, sums (in visitor order) and converts those
+//    whose visitors stored per-visitor partials (deterministic mode), and
+//    finishes dSink.
 // Both move 16-byte vectors per thread with consecutive threads on
 // consecutive 16-byte pieces of a row, so every warp access is coalesced.
 #include <cuda_bf16.h>
@@ -262,12 +264,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
     const int64_t t1 = imin(t0 + kTileQ, s.slot_q);
     if (t0 >= t1) return;
     int64_t z0 = t0;  // first row to zero
-    bool accumulated = false;
+    bool accumulated = false, from_slots = false;
+    int64_t n_vis = 0;
     if (t0 < s.len_q) {
-        int64_t first, n;
-        q_tile_visitors(g, s, j, first, n);
-        if (n > 0) z0 = s.len_q;
-        accumulated = n >= 3 && !a.deterministic;
+        int64_t first;
+        q_tile_visitors(g, s, j, first, n_vis);
+        if (n_vis > 0) z0 = s.len_q;
+        accumulated = n_vis >= 3 && !a.deterministic;
+        from_slots = n_vis >= 3 && a.deterministic && a.n_slots > 0;
     }
     const bool thd = g.layout == 1;
     uint16_t* dq = static_cast<uint16_t*>(a.dq);
@@ -279,6 +283,27 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
             const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8);
             const float4 x = src[0], y = src[1];
             const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+            uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
+                            h * a.dq_stride[2] + c * 8;
+            *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
+        }
+    }
+    if (from_slots) {
+        // deterministic mode: the visitors' partials, summed in visitor order
+        const int64_t e1 = imin(t1, s.len_q);
+        const int64_t nv = imin(n_vis, a.n_slots);
+        const float* base = a.dq_part + ((bi * g.h_q + h) * a.n_q_tiles + j) * a.n_slots * kTileQ * HD + c * 8;
+#pragma unroll 1
+        for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
+            const float* src = base + (i - t0) * HD;
+            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int64_t v = 0; v < nv; ++v) {
+                const float4 x = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[0];
+                const float4 y = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[1];
+                f[0] += x.x; f[1] += x.y; f[2] += x.z; f[3] += x.w;
+                f[4] += y.x; f[5] += y.y; f[6] += y.z; f[7] += y.w;
+            }
             uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
                             h * a.dq_stride[2] + c * 8;
             *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);

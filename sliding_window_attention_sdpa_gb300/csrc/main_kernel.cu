@@ -859,8 +859,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const int turn = static_cast<int>(it.t - first);
                 const bool single = nvis <= 1;
                 int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
-                // two visitors, or deterministic mode: hand the tile along in turn order
-                const bool relay = a.deterministic || nvis == 2;
+                // two visitors, or deterministic mode where no per-visitor slots
+                // apply (fewer than three visitors, or none allotted): hand the
+                // tile along in turn order
+                const bool relay = nvis == 2 || (a.deterministic && (nvis < 3 || a.n_slots == 0));
+                // deterministic mode otherwise: each visitor stores its own fp32
+                // partial (slot = turn), which the convert kernel sums in visitor
+                // order
+                const bool slots = a.deterministic && !relay;
                 const bool conv_now = single || (relay && turn == nvis - 1);
                 // accumulator write: a store for the first relay turn, else an add
                 const bool add = !(relay && turn == 0);
@@ -932,13 +938,21 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                         __uint_as_float(v[4 * i + 3]) * a.scale);
                 };
                 // Writes the staged fp32 columns [col0, col0 + 64) of the tile
-                // from thread 0 with two TMA boxes.
+                // from thread 0 with two TMA boxes: into the accumulator, or as
+                // this visitor's own partial (a store into its slot).
                 auto put_acc = [&](int col0) {
                     fence_proxy_async_smem();
                     named_bar_sync(kBarDq, 128);
                     if (r == 0) {
-                        tma_put(add, thd, &a.tm_acc, stg_s, col0, th, qrow, tb);
-                        tma_put(add, thd, &a.tm_acc, stg_s + kBlock16K, col0 + 32, th, qrow, tb);
+                        // a slot: a plain store at the slot's rows of the 3-D partials map
+                        const CUtensorMap* map = slots ? &a.tm_part : &a.tm_acc;
+                        // the slot's first row (n_slots covers every possible visitor)
+                        const int row = slots ? static_cast<int>((((it.bi * g.h_q + hh) * a.n_q_tiles + j) *
+                                                                      a.n_slots + turn) * kTileQ)
+                                              : qrow;
+                        const int hd = slots ? 0 : th;
+                        tma_put(add && !slots, thd || slots, map, stg_s, col0, hd, row, tb);
+                        tma_put(add && !slots, thd || slots, map, stg_s + kBlock16K, col0 + 32, hd, row, tb);
                         bulk_commit();
                     }
                 };
@@ -1053,7 +1067,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         } else {
                             stage_acc(0, v0);
                             stage_acc(1, v1);
-                            if (use_tma) put_acc(0);
+                            // a slot is a whole 128-row tile of the workspace
+                            if (use_tma || slots) put_acc(0);
                             else apply(0);
                         }
                     }
@@ -1095,12 +1110,18 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             tmem_ld32(tmem + C::kColDQ + lane_off + rd * 64 + 32, v);
                             tmem_ld_wait();
                             stage_acc(1, v);
-                            if (use_tma && !conv_now) {
+                            if ((use_tma || slots) && !conv_now) {
                                 fence_proxy_async_smem();
                                 named_bar_sync(kBarDq, 128);
                                 if (r == 0 && go) {
-                                    tma_put(add, thd, &a.tm_acc, stg_s, rd * 64, th, qrow, tb);
-                                    tma_put(add, thd, &a.tm_acc, stg_s + kBlock16K, rd * 64 + 32, th, qrow, tb);
+                                    const CUtensorMap* map = slots ? &a.tm_part : &a.tm_acc;
+                                    const int row = slots ? static_cast<int>((((it.bi * g.h_q + hh) * a.n_q_tiles +
+                                                                                j) * a.n_slots + turn) * kTileQ)
+                                                          : qrow;
+                                    const int hd = slots ? 0 : th;
+                                    tma_put(add && !slots, thd || slots, map, stg_s, rd * 64, hd, row, tb);
+                                    tma_put(add && !slots, thd || slots, map, stg_s + kBlock16K, rd * 64 + 32, hd,
+                                            row, tb);
                                     bulk_commit();
                                 }
                             } else if (go) {

@@ -37,6 +37,10 @@ struct WsLayout {
     size_t stats;       // float2 (LSE * log2(e), D) per row, [b][h_q][n_q_tiles * 128]
     size_t sems;        // int32 [b][h_q][n_q_tiles]
     size_t dsink_part;  // fp32 [h_q][n_row_blocks]
+    // deterministic mode, q-tiles with three or more visitors: one fp32 partial
+    // dQ tile per visitor, [b][h_q][n_q_tiles][n_slots][128][d] (0: relay only)
+    size_t dq_part;
+    int64_t n_slots;
     size_t total;
     int64_t n_sems;
     int64_t n_row_blocks;
@@ -86,6 +90,9 @@ struct MainArgs {
     // dtype, 64 x 1 x 128 boxes) and the fp32 dQ accumulator (32 x 1 x 128
     // boxes), all with the 128-byte swizzle.
     CUtensorMap tm_dq, tm_dk, tm_dv, tm_acc;
+    // the per-visitor partial dQ tiles (fp32, 3-D (d, 1, rows), 32 x 1 x 128
+    // boxes, 128-byte swizzle); used when n_slots > 0
+    CUtensorMap tm_part;
     Geometry g;
     const void *q, *k, *v, *dout;
     const float2* stats;      // per-row (LSE * log2(e), D), tile-aligned (see PreArgs)
@@ -102,12 +109,16 @@ struct MainArgs {
     float scale;
     float scale_log2;         // scale * log2(e)
     int32_t deterministic;
+    int64_t n_slots;          // per-visitor partial dQ slots (deterministic mode), 0: relay
     int64_t timeout_ns;
 };
 
 struct CvtArgs {
     Geometry g;
     const float* dq_acc;  // converted here on q-tiles that took unordered atomics
+    const float* dq_part; // per-visitor partials, summed here in visitor order
+    int64_t n_slots;      // 0: no partial slots
+    int64_t n_q_tiles;
     int32_t deterministic;
     void* dq;
     int64_t dq_stride[3];

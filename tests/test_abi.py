@@ -58,6 +58,27 @@ def base_params(**kw):
     return p
 
 
+def test_deterministic_slots_workspace():
+    """Deterministic mode 1 adds one fp32 128 x d tile per (sequence, q-head,
+    q-tile, possible visitor) when a q-tile can have three or more visitors;
+    mode 2 (relay only) and two-visitor windows add nothing."""
+    wide = dict(window_left=-1, s_q=512, s_kv=512)
+    base = swa.sdpa_bwd_workspace_bytes(base_params(**wide))
+    relay = swa.sdpa_bwd_workspace_bytes(base_params(deterministic=2, **wide))
+    slots = swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1, **wide))
+    assert relay == base
+    p = base_params(**wide)
+    # 4 kv-tiles may visit each of the 4 q-tiles
+    extra = p.b * p.h_q * 4 * 4 * 128 * p.d * 4
+    assert base + extra <= slots <= base + extra + 256
+    # W = 32 over 4 kv-tiles: up to three kv-tiles may reach a q-tile's rows
+    s512 = dict(s_q=512, s_kv=512)
+    assert (swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1, **s512))
+            > swa.sdpa_bwd_workspace_bytes(base_params(**s512)))
+    # ... but only two of the 2 kv-tiles of 256 rows; no slots
+    assert swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1)) == swa.sdpa_bwd_workspace_bytes(base_params())
+
+
 def test_workspace_bytes():
     p = base_params()
     n = swa.sdpa_bwd_workspace_bytes(p)
@@ -77,7 +98,7 @@ def test_workspace_bytes():
     ("h_kv", 3, swa.SDPA_ERR_INVALID_ARG, "multiple of h_kv"),
     ("d", 80, swa.SDPA_ERR_UNSUPPORTED, "d=80"),
     ("window_left", -5, swa.SDPA_ERR_INVALID_ARG, "window_left"),
-    ("deterministic", 2, swa.SDPA_ERR_INVALID_ARG, "deterministic"),
+    ("deterministic", 3, swa.SDPA_ERR_INVALID_ARG, "deterministic"),
     ("sink", 4096, swa.SDPA_ERR_INVALID_ARG, "dsink"),
     ("scale", 0.0, swa.SDPA_ERR_INVALID_ARG, "scale"),
 ])
@@ -126,10 +147,13 @@ def test_kernel_launch_count():
     # with length arrays rows past a sequence's length may need zeros
     assert swa.sdpa_bwd_kernel_launches(base_params(seq_q_lens=4096)) == 3
     # no window over 512 rows: q-tile 3 has four visitors, added with atomics
-    # unless deterministic (then the relay's last turn converts)
+    # (converted by the convert kernel); deterministic mode 1 keeps a partial
+    # per visitor, summed by the convert kernel; mode 2 passes the tile along
+    # the relay, whose last turn converts
     wide = dict(window_left=-1, s_q=512, s_kv=512)
     assert swa.sdpa_bwd_kernel_launches(base_params(**wide)) == 3
-    assert swa.sdpa_bwd_kernel_launches(base_params(deterministic=1, **wide)) == 2
+    assert swa.sdpa_bwd_kernel_launches(base_params(deterministic=1, **wide)) == 3
+    assert swa.sdpa_bwd_kernel_launches(base_params(deterministic=2, **wide)) == 2
     # bottom-right, 128 queries against 512 keys, W=32: q-tile 0 is visited by
     # kv-tiles 2 and 3 only
     br = dict(mask_mode=swa.SDPA_MASK_BOTTOM_RIGHT, s_q=128, s_kv=512)

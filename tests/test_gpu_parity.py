@@ -81,6 +81,28 @@ def test_deterministic_is_bitwise_repeatable_and_matches_nondet():
         compare(name, a, b.double().cpu().numpy(), "bf16")
 
 
+def test_deterministic_slots_and_relay():
+    """Deterministic mode with three or more visitors per q-tile: mode 1 keeps
+    one fp32 partial per visitor and the convert kernel sums them in visitor
+    order; mode 2 passes the tile along the relay. Both match the oracle and
+    are bitwise repeatable; they add the same partials in the same order, up
+    to the relay's fused last add (a last-bit difference before rounding)."""
+    case = Case("det_none_w300_r100_gqa4x2_sink", 2, 4, 2, 900, 900, 64, "none", 300, 100,
+                sink=True, det=True, seed=22)
+    bt = build(case)
+    slots = [run_gpu(bt, deterministic=1) for _ in range(2)]
+    relay = [run_gpu(bt, deterministic=2) for _ in range(2)]
+    for runs in (slots, relay):
+        for a, b in zip(runs[0], runs[1]):
+            assert torch.equal(a, b)
+        check_all(bt, runs[0])
+    for name, a, b in zip(("dq", "dk", "dv", "dsink"), slots[0], relay[0]):
+        compare(name, a, b.double().cpu().numpy(), "bf16")
+    # dK, dV and dSink do not depend on the dQ scheme
+    for a, b in zip(slots[0][1:], relay[0][1:]):
+        assert torch.equal(a, b)
+
+
 def test_padding_values_never_leak():
     """NaN in every padded row of Q, K, V, O, dO and LSE: results in the valid
     region are unchanged and padded rows get zero gradients."""
