@@ -208,12 +208,12 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "17edf0fa50583237", "bytes": 248640512},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "001301e903aa3bc4", "bytes": 248899328},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
 FWD_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "2e74010e10ff2ca6", "bytes": 114754304},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "27a2912ff5339117", "bytes": 113857792},
 }
 FWD_SOURCES = ("fwd_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 
