@@ -202,7 +202,10 @@ sdpa_status_t sdpa_bwd_check_status(const void *workspace, void *stream);
  * exits). It calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Size limit: a problem whose sdpa_bwd_workspace_bytes() exceeds
  *    SDPA_BWD_NO_ALLOC_MAX_BYTES is rejected with SDPA_ERR_WORKSPACE before
- *    anything is enqueued; use the workspace entry points for it.
+ *    anything is enqueued; use the workspace entry points for it. In
+ *    deterministic mode 1 the per-visitor dQ slots are dropped first (the call
+ *    runs as mode 2, the relay: also bitwise repeatable) when that makes the
+ *    problem fit.
  *  - Set-up: the first call on a device (with that device current) looks up
  *    the array's device address once; make that first call before any stream
  *    capture.

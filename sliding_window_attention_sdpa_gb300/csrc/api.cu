@@ -581,11 +581,19 @@ sdpa_status_t no_alloc_scratch(void** out)
 
 extern "C" {
 
-sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params* p, void* stream)
+sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params* params, void* stream)
 {
-    sdpa_status_t st = check_shape(p);
+    sdpa_status_t st = check_shape(params);
     if (st != SDPA_OK) return st;
-    const size_t need = layout_of(p).total;
+    // deterministic mode 1 whose per-visitor dQ slots do not fit the scratch
+    // uses the relay (mode 2): the same bitwise-repeatable sums, no slots
+    sdpa_bwd_params local = *params;
+    size_t need = layout_of(&local).total;
+    if (need > SDPA_BWD_NO_ALLOC_MAX_BYTES && local.deterministic == 1) {
+        local.deterministic = 2;
+        need = layout_of(&local).total;
+    }
+    const sdpa_bwd_params* p = &local;
     if (need > SDPA_BWD_NO_ALLOC_MAX_BYTES)
         return fail(SDPA_ERR_WORKSPACE,
                     "sdpa_bwd_no_alloc: this problem needs %zu bytes of scratch, more than the fixed "

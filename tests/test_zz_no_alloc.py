@@ -35,6 +35,24 @@ def test_oversized_problem_is_refused_on_the_host():
     assert str(need) in msg and str(swa.SDPA_BWD_NO_ALLOC_MAX_BYTES) in msg
 
 
+def test_deterministic_slots_give_way_to_the_relay():
+    """A deterministic problem whose per-visitor dQ slots do not fit the fixed
+    scratch, but whose relay-only workspace does, passes the size check (it
+    runs in relay-only mode); only a later step can refuse it here (no device
+    or no real tensors)."""
+    swa._build.build()
+    p = swa.SdpaBwdParams()
+    p.dtype, p.layout, p.mask_mode = swa.SDPA_BF16, swa.SDPA_BSHD, swa.SDPA_MASK_TOP_LEFT
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 1, 4, 4, 4096, 4096, 64
+    p.window_left, p.window_right, p.scale = 1024, -1, 0.125
+    p.deterministic = 1
+    assert swa.sdpa_bwd_workspace_bytes(p) > swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+    p.deterministic = 2
+    assert swa.sdpa_bwd_workspace_bytes(p) <= swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+    p.deterministic = 1
+    assert swa.sdpa_bwd_no_alloc(p, None) != swa.SDPA_ERR_WORKSPACE
+
+
 @pytest.mark.gpu
 def test_no_alloc_matches_workspace_entry_points_twice():
     if not torch.cuda.is_available():
