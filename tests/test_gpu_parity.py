@@ -57,6 +57,13 @@ SMALL = [
     Case("tl_w700_gqa4x2_sink_s900_det", 1, 4, 2, 900, 900, 64, "tl", 700, sink=True, det=True,
          seed=17),
     Case("none_w300_d128_f16", 1, 2, 2, 700, 700, 128, "none", 300, dtype="f16", seed=18),
+    # deterministic with three or more visitors: per-visitor dQ slots, at d = 128
+    # and with THD tiles that end inside a slot
+    Case("br_w300_gqa4x2_d128_det_slots", 1, 4, 2, 700, 700, 128, "br", 300, det=True, seed=24),
+    Case("thd_none_w300_det_slots", 0, 4, 2, 0, 0, 64, "none", 300, layout="thd",
+         thd_lens=[390, 64, 1000], slot_align=8, det=True, seed=23),
+    Case("br_nonsquare_q128_kv1100_w800_det_slots", 2, 8, 2, 128, 1100, 64, "br", 800, det=True,
+         seed=25),
 ]
 
 
