@@ -376,7 +376,7 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
     copy3(a.do_stride, p->do_stride);
     a.dq_acc = at<float>(ws, w.dq_acc);
     a.deterministic = p->deterministic;
-    a.stats = at<float2>(ws, w.stats);
+    a.stats = at<float>(ws, w.stats);
     a.stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
     a.status = at<int32_t>(ws, w.status);
     a.sems = at<int32_t>(ws, w.sems);
@@ -415,7 +415,7 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     a.k = p->k;
     a.v = p->v;
     a.dout = p->dout;
-    a.stats = at<float2>(ws, w.stats);
+    a.stats = at<float>(ws, w.stats);
     a.stats_row = ((p->s_q + swa::kTileQ - 1) / swa::kTileQ) * swa::kTileQ;
     a.dq_acc = at<float>(ws, w.dq_acc);
     a.dq = p->dq;

@@ -205,14 +205,17 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
         }
         if (unit && half == 0) {
             // per-row statistics for the main kernel, one slot for every row of
-            // every q-tile: (LSE * log2(e), D); rows past the length or that
-            // attend nothing get (+inf, 0) so that P = 0 there
-            float l2 = INFINITY, ds = 0.f;
+            // every q-tile: -LSE * log2(e) and -D in the tile's two 128-float
+            // runs; rows past the length or that attend nothing get (-inf, 0)
+            // so that P = 0 there
+            float nl2 = -INFINITY, ds = 0.f;
             if (valid && lse != -INFINITY) {
-                l2 = lse * 1.4426950408889634f;
+                nl2 = -(lse * 1.4426950408889634f);
                 if (with_sink) ds = -expf(a.sink[h] - lse) * part;
             }
-            a.stats[(b.bi * g.h_q + h) * a.stats_row + i] = make_float2(l2, valid ? part : 0.f);
+            float* srow = a.stats + 2 * ((b.bi * g.h_q + h) * a.stats_row + (i & ~int64_t(kTileQ - 1))) + (i & (kTileQ - 1));
+            srow[0] = nl2;
+            srow[kTileQ] = valid ? -part : 0.f;
             if (with_sink) red[(j & 1) * 256 + hl * rows_n + r] = ds;
         }
         __syncthreads();   // ring entry st is read; dSink terms are written

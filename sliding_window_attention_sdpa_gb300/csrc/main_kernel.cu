@@ -88,7 +88,7 @@ struct Cfg {
     // row at d = 64, half of it at d = 128), or the whole 16-bit dQ tile
     static constexpr int kDqCols = 64;
     static constexpr uint32_t kDqStage = kDS + kDsBufs * 32768;
-    static constexpr uint32_t kStat = kDqStage + 128 * kDqCols * 4;  // kStages x 128 float2
+    static constexpr uint32_t kStat = kDqStage + 128 * kDqCols * 4;  // kStages x (128 -LSE log2, 128 -D)
     static constexpr uint32_t kBars = kStat + kStages * 1024;   // mbarriers
     static constexpr uint32_t kMisc = kBars + 256;              // tmem slot, flags, deferred epilogue
     static constexpr uint32_t kBytes = kMisc + 128;
@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     tma_tile<HD>(sbase + C::kDO + st * C::kTile, &a.tm_do, bar(kQFull0 + st), thd,
                                  (int)hh, qrow, (int)it.bi);
                     bulk_load(sbase + C::kStat + st * 1024,
-                              a.stats + (static_cast<int64_t>(it.bi) * g.h_q + hh) * a.stats_row +
-                                  static_cast<int64_t>(j) * kTileQ,
+                              a.stats + 2 * ((static_cast<int64_t>(it.bi) * g.h_q + hh) * a.stats_row +
+                                             static_cast<int64_t>(j) * kTileQ),
                               1024, bar(kQFull0 + st));
                     SWA_TRACE(13, q_it);
                 }
@@ -721,7 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         SWA_TRACE(warp == kWarpSoft0 ? 5 : 7, q_it);
                     ++s_it;
                     tc_fence_after();
-                    const float2* stv = reinterpret_cast<const float2*>(sm + C::kStat + st * 1024);
+                    // the q-tile's statistics: 128 x -LSE * log2(e), then 128 x -D
+                    const float* nls = reinterpret_cast<const float*>(sm + C::kStat + st * 1024);
+                    const float* nds = nls + kTileQ;
+                    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
                     const int64_t q0 = j * kTileQ;
                     const int c_lo = static_cast<int>(imax(i_lo - q0, 0));
                     const int c_hi = static_cast<int>(imin(i_hi - q0, 127));
@@ -741,31 +744,37 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             tmem_ld16(tmem + C::kColS + lane_off + c0, sv);
                             tmem_ld16(tmem + C::kColDP + lane_off + c0, dpv);
                             tmem_ld_wait();
+                            // Column pairs in packed fp32x2 arithmetic: x = s * scale * log2(e)
+                            // - LSE * log2(e), P = 2^x, dS = P (dP - D).
                             if (full) {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
-                                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -stv[c0 + e].x));
-                                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -stv[c0 + e + 1].x));
+                                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                                sc2, *reinterpret_cast<const float2*>(nls + c0 + e));
+                                    const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                                    const float2 t = __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                                                *reinterpret_cast<const float2*>(nds + c0 + e));
+                                    const float2 d = __fmul2_rn(make_float2(p0, p1), t);
                                     pk[e >> 1] = pack2<BF16>(p0, p1);
-                                    dk[e >> 1] = pack2<BF16>(p0 * (__uint_as_float(dpv[e]) - stv[c0 + e].y),
-                                                             p1 * (__uint_as_float(dpv[e + 1]) - stv[c0 + e + 1].y));
+                                    dk[e >> 1] = pack2<BF16>(d.x, d.y);
                                 }
                             } else {
+                                // masked columns: x = -inf gives P = 0; dS is selected to 0
+                                // (dP may be NaN there: padding rows of V are not read-safe)
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
-                                    float p2[2], d2[2];
-#pragma unroll
-                                    for (int u = 0; u < 2; ++u) {
-                                        const int c = c0 + e + u;
-                                        const bool att = c >= c_lo && c <= c_hi;
-                                        const float p = att ? ex2_approx(fmaf(__uint_as_float(sv[e + u]),
-                                                                             a.scale_log2, -stv[c].x))
-                                                            : 0.f;
-                                        p2[u] = p;
-                                        d2[u] = att ? p * (__uint_as_float(dpv[e + u]) - stv[c].y) : 0.f;
-                                    }
-                                    pk[e >> 1] = pack2<BF16>(p2[0], p2[1]);
-                                    dk[e >> 1] = pack2<BF16>(d2[0], d2[1]);
+                                    const int c = c0 + e;
+                                    const bool att0 = c >= c_lo && c <= c_hi, att1 = c + 1 >= c_lo && c + 1 <= c_hi;
+                                    float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                          sc2, *reinterpret_cast<const float2*>(nls + c));
+                                    x.x = att0 ? x.x : -INFINITY;
+                                    x.y = att1 ? x.y : -INFINITY;
+                                    const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                                    const float2 t = __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                                                *reinterpret_cast<const float2*>(nds + c));
+                                    const float2 d = __fmul2_rn(make_float2(p0, p1), t);
+                                    pk[e >> 1] = pack2<BF16>(p0, p1);
+                                    dk[e >> 1] = pack2<BF16>(att0 ? d.x : 0.f, att1 ? d.y : 0.f);
                                 }
                             }
                         }

@@ -34,7 +34,8 @@ constexpr int kStatusBadLengths = 5;
 struct WsLayout {
     size_t status;      // int32 status, int32 ticket counter
     size_t dq_acc;      // fp32 [rows_q][h_q][d]
-    size_t stats;       // float2 (LSE * log2(e), D) per row, [b][h_q][n_q_tiles * 128]
+    size_t stats;       // fp32 per-row statistics, [b][h_q][n_q_tiles][2][128]: per q-tile
+                        // 128 x -LSE * log2(e), then 128 x -D
     size_t sems;        // int32 [b][h_q][n_q_tiles]
     size_t dsink_part;  // fp32 [h_q][n_row_blocks]
     // deterministic mode, q-tiles with three or more visitors: one fp32 partial
@@ -73,8 +74,12 @@ struct PreArgs {
     int64_t o_stride[3], do_stride[3];
     float* dq_acc;       // zeroed here on q-tiles that take unordered atomics
     int32_t deterministic;
-    float2* stats;       // (LSE * log2(e) or +inf where nothing is attended, D)
-    int64_t stats_row;   // entries per (sequence, q-head): n_q_tiles * 128
+    // Per q-tile of a (sequence, q-head): 128 x -LSE * log2(e) (-inf where a row
+    // attends nothing or lies past the length), then 128 x -D (0 there). Negated
+    // and split so that the main kernel forms each pair of exponent arguments
+    // with one packed fp32x2 FMA and each pair of (dP - D) with one packed add.
+    float* stats;
+    int64_t stats_row;   // rows per (sequence, q-head): n_q_tiles * 128 (2 floats each)
     int32_t* status;     // status + ticket (2 ints)
     int32_t* sems;
     int64_t n_sems;
@@ -95,7 +100,7 @@ struct MainArgs {
     CUtensorMap tm_part;
     Geometry g;
     const void *q, *k, *v, *dout;
-    const float2* stats;      // per-row (LSE * log2(e), D), tile-aligned (see PreArgs)
+    const float* stats;       // per q-tile -LSE * log2(e) and -D runs (see PreArgs)
     int64_t stats_row;
     float* dq_acc;            // fp32 partial sums of q-tiles with several visitors
     void* dq;                 // dQ output (I/O dtype), written by each q-tile's last visitor
