@@ -301,7 +301,9 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
     as a training loop would feed its batches: the copy of step k + 1's inputs
     and the read of step k - 1's results run while step k computes. Device
     input buffers alternate between two sets. Returns (ms per step, host ->
-    device bytes per step, device -> host bytes per step).
+    device bytes per step, device -> host bytes per step, link rates): the
+    link rates are the same copies timed alone after the timed region, each
+    direction on its own (GB/s), which bound the pipelined step from below.
     """
     import sliding_window_attention_sdpa_gb300 as swa
     names = (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)
@@ -344,7 +346,24 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
         one(warmup + k)
     b.record(s_out)
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+    ms = a.elapsed_time(b) / steps
+
+    def alone(stream, pairs, nbytes, reps=5):
+        out = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1))
+        return nbytes / (sorted(out)[reps // 2] * 1e-3) / 1e9
+
+    link = {"h2d_gbs": alone(s_in, list(zip(dev_in[0], host_in)), h2d),
+            "d2h_gbs": alone(s_out, list(zip(host_out, (prob.dq, prob.dk, prob.dv))), d2h)}
+    return ms, h2d, d2h, link
 
 
 def cpu_oracle_step(name: str, nthreads: int, units=None):
@@ -482,7 +501,7 @@ def main():
     with ClockSampler(local) as clk:
         total, main_ms = time_device(prob, args.steps, args.warmup)
         torch.cuda.synchronize()
-        e2e_ms, h2d, d2h = time_e2e(prob, max(3, args.steps), 2)
+        e2e_ms, h2d, d2h, link = time_e2e(prob, max(3, args.steps), 2)
         fwd_ms = time_forward(prob, args.steps, args.warmup)
     step_ms = sum(total) / len(total)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
@@ -518,7 +537,9 @@ def main():
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_max,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "overlap": "step k+1's host->device copy and step k-1's device->host read run "
-                           "during step k (three streams)"},
+                           "during step k (three streams)",
+                # the step's copies timed alone, one direction at a time
+                "link_gbs": {k: round(v, 1) for k, v in link.items()}},
         "gpu_launches": prob.launches_per_step() * args.steps,
         "clocks": clk.summary(),
         # the forward (O, LSE) on the same workload, timed after the backward's
