@@ -16,7 +16,8 @@ dirty line of the flush is left for the step's first kernel to write back
   e2e        the same metric through the public API from pinned host buffers,
              host->device copies of Q, K, V, O, dO, LSE and the device->host
              read of dQ, dK, dV inside every timed step (consecutive steps'
-             copies and compute overlap on three streams)
+             copies and compute overlap on three streams); link_gbs holds the
+             same copies timed alone, one direction at a time
   roofline   the main kernel: algorithmic bytes per launch / its mean duration
              (CUDA events on the launching stream) against measured HBM peak
   cpu_baseline  the fp64 CPU oracle on the same workload (host cores)
@@ -208,12 +209,12 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "001301e903aa3bc4", "bytes": 248899328},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "9f23aee864093a0a", "bytes": 248809728},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
 FWD_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "27a2912ff5339117", "bytes": 113857792},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "178f41b8bced324b", "bytes": 114658304},
 }
 FWD_SOURCES = ("fwd_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 
