@@ -157,10 +157,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str | None = None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples; the JSON line carries their summary
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -473,6 +475,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log-dir", default=None,
+                    help="folder for the raw nvidia-smi clock samples (default: the temp folder)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -499,7 +503,7 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clock_log_dir) as clk:
         total, main_ms = time_device(prob, args.steps, args.warmup)
         torch.cuda.synchronize()
         e2e_ms, h2d, d2h, link = time_e2e(prob, max(3, args.steps), 2)
