@@ -120,10 +120,12 @@ typedef struct sdpa_bwd_params {
 /*
  * Workspace size in bytes for `params` (0 on invalid params; see
  * sdpa_bwd_last_error). The workspace holds the fp32 dQ accumulator, D = rowsum
- * (dO*O), the relay counters, the dSink partials, the status word and, in
- * deterministic mode 1 when a q-tile can have three or more visitors, up to
- * 2 GiB of per-visitor partial dQ tiles. It must be 256-byte aligned device
- * memory; its contents need no initialisation.
+ * (dO*O), the relay counters, the dSink partials, the status word, at d = 64
+ * the main kernel's table of decoded work items (152 bytes per (batch,
+ * kv-head, kv-tile), rewritten by every sdpa_bwd call) and, in deterministic mode 1 when
+ * a q-tile can have three or more visitors, up to 2 GiB of per-visitor partial
+ * dQ tiles. It must be 256-byte aligned device memory; its contents need no
+ * initialisation.
  */
 size_t sdpa_bwd_workspace_bytes(const sdpa_bwd_params *params);
 
@@ -141,7 +143,9 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params *params, void *workspace
 
 /*
  * Main backward ("main" kernel; PR #866 clamp and relay): one work item per
- * (kv-tile, kv-head, batch). For each q-head of the kv-head's group and each
+ * (kv-tile, kv-head, batch); at d = 64 each CTA first decodes its items
+ * (sequence lengths, clamped q-tile range) into the workspace's item table,
+ * which its roles then read. For each q-head of the kv-head's group and each
  * q-tile in the clamped range [q_lo, q_hi) (swept from the top down) it
  * recomputes P and dS and accumulates dV, dK in tensor memory, so the GQA/MQA
  * group sum (PR #557) happens in place, in head order; stores dK, dV.

@@ -152,6 +152,11 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     off = align256(off + static_cast<size_t>(w.n_sems) * 4);
     w.dsink_part = off;
     if (p->sink != nullptr) off = align256(off + static_cast<size_t>(p->h_q) * w.n_row_blocks * 4);
+    // the main kernel's table of decoded work items (d = 64)
+    w.items = off;
+    if (p->d == 64)
+        off = align256(off + static_cast<size_t>(p->b) * p->h_kv * ((p->s_kv + swa::kTileKV - 1) / swa::kTileKV) *
+                                 swa::kItemBytes);
     // Deterministic mode (1): q-tiles that three or more kv-tiles visit keep one
     // fp32 partial per visitor, summed in visitor order by the convert kernel,
     // instead of passing one tile along the relay, when the slots fit the cap.
@@ -479,6 +484,7 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     } else {
         a.tm_part = a.tm_k;
     }
+    a.items = at<uint8_t>(ws, w.items);
     return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
 }
 

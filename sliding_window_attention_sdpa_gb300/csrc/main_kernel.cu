@@ -55,6 +55,8 @@ namespace swa {
 namespace {
 
 constexpr int kThreads = 512;
+// The item table is used when a CTA has at most this many items.
+constexpr int64_t kItemTableMaxPerCta = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBlock16K = 128 * 128;  // one 64-column block of a 128-row tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -226,6 +228,12 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, u
     }
 }
 
+// Starts moving the 128-byte line holding `p` into this SM's L1.
+__device__ __forceinline__ void prefetch_l1(const void* p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -284,6 +292,8 @@ struct Item {
         }
     }
 };
+
+static_assert(sizeof(Item) == kItemBytes, "the host sizes the item table with kItemBytes");
 
 // One work item's dK/dV store, as the softmax group runs it (d = 64 defers it
 // to after the next item's first q-tile, keeping it in shared memory).
@@ -400,8 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         tmem_alloc(sbase + C::kMisc, kTmemCols);
         tmem_relinquish();
     }
+    // d = 64: every item of this CTA is decoded once, by all threads in
+    // parallel, into the item table, and the roles read their items from it.
+    // Decoding in each role at each item boundary ran as cold code on the
+    // critical path (about 1 K cycles per item on the softmax warps), and an
+    // item has only a few q-tile steps there. At d = 128 (no look-ahead, more
+    // registers live) the roles decode in place: the table's copies cost more
+    // than the decode.
+    Item* items = static_cast<Item*>(a.items);
+    const bool use_items = C::kAhead && a.use_items != 0;
+    if (use_items)
+        for (int64_t item = blockIdx.x + static_cast<int64_t>(tid) * gridDim.x; item < n_items;
+             item += static_cast<int64_t>(kThreads) * gridDim.x)
+            items[item] = decode(a, cnt, item);
+    auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode(a, cnt, i); };
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();   // also publishes the item table to the CTA
     tc_fence_after();
     const uint32_t tmem = misc[0];
     volatile uint32_t* abort_flag = misc + 1;
@@ -427,7 +451,18 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
             for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-                const Item it = decode(a, cnt, item);
+                const Item it = item_at(item);
+                if (use_items) {
+                    // The next two items' records toward this SM's L1 (every role
+                    // reads them later than this warp): written at the kernel's
+                    // start, they may have left the L2 by then.
+                    for (int64_t nx = item + gridDim.x; nx < n_items && nx <= item + 2 * gridDim.x; nx += gridDim.x) {
+                        const char* rec = reinterpret_cast<const char*>(items + nx);
+                        prefetch_l1(rec);
+                        prefetch_l1(rec + kItemBytes / 2);
+                        prefetch_l1(rec + kItemBytes - 1);
+                    }
+                }
                 if (!it.has_work) continue;
                 const int ks = kv_it % C::kKvStages;
                 if (!wait(kKvEmpty0 + ks, ((kv_it / C::kKvStages) & 1) ^ 1)) break;
@@ -536,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode(a, cnt, item);
+            const Item it = item_at(item);
             if (!it.has_work) continue;
             const int ks = kv_it % C::kKvStages;
             if (!(ok = wait_warp(kKvFull0 + ks, (kv_it / C::kKvStages) & 1))) break;
@@ -693,10 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 *reinterpret_cast<uint4*>(dst) = w;
             }
         };
-        // The next item is decoded right after this one's last P^T hand-off, so
-        // that its (cold) decode overlaps the wait for the last gradients.
-        auto decode_at = [&](int64_t i) -> Item { return decode(a, cnt, i < n_items ? i : blockIdx.x); };
-        Item it = decode(a, cnt, blockIdx.x), nxt;
+        // The next item's record is read right after this one's last P^T
+        // hand-off, so that the load overlaps the epilogue bookkeeping.
+        auto decode_at = [&](int64_t i) -> Item { return item_at(i < n_items ? i : blockIdx.x); };
+        Item it = item_at(blockIdx.x), nxt;
         bool have_nxt = false;
         for (int64_t item = blockIdx.x; item < n_items;
              item += gridDim.x, it = have_nxt ? nxt : decode_at(item), have_nxt = false) {
@@ -858,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         uint32_t dq_it = 0, ld_it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode(a, cnt, item);
+            const Item it = item_at(item);
             if (!it.has_work) continue;
             for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, it.advance(j, hh)) {
                 // this visit's bookkeeping first, while the dQ contraction runs
@@ -1184,7 +1219,9 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t grid = items < sms ? items : sms;
-    kern<<<static_cast<unsigned>(grid), kThreads, bytes, s>>>(a);
+    MainArgs b = a;
+    b.use_items = items <= kItemTableMaxPerCta * grid;
+    kern<<<static_cast<unsigned>(grid), kThreads, bytes, s>>>(b);
     return cudaGetLastError();
 }
 

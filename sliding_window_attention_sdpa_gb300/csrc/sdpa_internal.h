@@ -26,6 +26,9 @@ inline __host__ __device__ PreTile pre_tile(int64_t h_q, int64_t d)
     while (rows * 2 * heads <= units && rows < 128) rows *= 2;
     return PreTile{heads, rows};
 }
+// Bytes of one decoded main-kernel work item (the kernel checks its record
+// type against this).
+constexpr size_t kItemBytes = 152;
 constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;
@@ -42,6 +45,9 @@ struct WsLayout {
     // dQ tile per visitor, [b][h_q][n_q_tiles][n_slots][128][d] (0: relay only)
     size_t dq_part;
     int64_t n_slots;
+    // d = 64: the main kernel's decoded work items, one kItemBytes record per
+    // (sequence, kv-head, kv-tile), written and read by that launch only
+    size_t items;
     size_t total;
     int64_t n_sems;
     int64_t n_row_blocks;
@@ -116,6 +122,12 @@ struct MainArgs {
     int32_t deterministic;
     int64_t n_slots;          // per-visitor partial dQ slots (deterministic mode), 0: relay
     int64_t timeout_ns;
+    // d = 64: n_items = b * h_kv * n_kv_tiles records of kItemBytes (8-byte
+    // aligned); each CTA decodes its own items into it once, before its roles
+    // start, when use_items is set (the launcher sets it when a CTA has few
+    // items; with many, the roles decode in place)
+    void* items;
+    int32_t use_items;
 };
 
 struct CvtArgs {
