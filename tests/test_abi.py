@@ -91,6 +91,9 @@ def test_workspace_bytes():
     n_kv_tiles = (p.s_kv + 127) // 128
     table_diff = p.b * (p.h_kv - 2) * n_kv_tiles * 152
     assert abs((n - swa.sdpa_bwd_workspace_bytes(g)) - table_diff) < 256
+    # d = 128 decodes its items in place: no table, so GQA changes nothing
+    n128 = swa.sdpa_bwd_workspace_bytes(base_params(d=128))
+    assert n128 > 0 and swa.sdpa_bwd_workspace_bytes(base_params(d=128, h_kv=2)) == n128
     assert swa.sdpa_bwd_workspace_bytes(base_params(d=96)) == 0
     assert "d=96" in swa.last_error()
 
