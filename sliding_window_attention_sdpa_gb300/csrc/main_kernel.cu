@@ -410,13 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         tmem_alloc(sbase + C::kMisc, kTmemCols);
         tmem_relinquish();
     }
-    // d = 64: every item of this CTA is decoded once, by all threads in
-    // parallel, into the item table, and the roles read their items from it.
-    // Decoding in each role at each item boundary ran as cold code on the
-    // critical path (about 1 K cycles per item on the softmax warps), and an
-    // item has only a few q-tile steps there. At d = 128 (no look-ahead, more
-    // registers live) the roles decode in place: the table's copies cost more
-    // than the decode.
+    // d = 64 with few items per CTA (the launcher sets use_items): every item
+    // of this CTA is decoded once, by all threads in parallel, into the item
+    // table, and the roles read their items from it. Decoding in each role at
+    // each item boundary ran as cold code on the critical path (about 1 K
+    // cycles per item on the softmax warps), and an item has only a few q-tile
+    // steps there. With many items per CTA, and at d = 128 (no look-ahead,
+    // more registers live), the roles decode in place: there the table was
+    // slower.
     Item* items = static_cast<Item*>(a.items);
     const bool use_items = C::kAhead && a.use_items != 0;
     if (use_items)
@@ -453,9 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const Item it = item_at(item);
                 if (use_items) {
-                    // The next two items' records toward this SM's L1 (every role
-                    // reads them later than this warp): written at the kernel's
-                    // start, they may have left the L2 by then.
+                    // The next two items' records toward this SM's L1, ahead of
+                    // the roles' reads (every role reaches them after this warp).
                     for (int64_t nx = item + gridDim.x; nx < n_items && nx <= item + 2 * gridDim.x; nx += gridDim.x) {
                         const char* rec = reinterpret_cast<const char*>(items + nx);
                         prefetch_l1(rec);
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                 }
                             } else {
                                 // masked columns: x = -inf gives P = 0; dS is selected to 0
-                                // (dP may be NaN there: padding rows of V are not read-safe)
+                                // (dP may be NaN there: padding rows need not be finite)
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
                                     const int c = c0 + e;
