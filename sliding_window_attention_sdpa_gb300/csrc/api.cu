@@ -116,19 +116,30 @@ sdpa_status_t check_device_ptr(const char* name, const void* ptr, bool required,
 int64_t rows_q(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_q : p->b * p->s_q; }
 int64_t rows_kv(const sdpa_bwd_params* p) { return p->layout == SDPA_THD ? p->total_kv : p->b * p->s_kv; }
 
-// Largest number of kv-tiles that can visit one q-tile: the keys a q-tile's
-// rows attend span tile_q + W_left + W_right positions (plus one tile for the
-// alignment); all kv-tiles when the window is unbounded on either side.
-int64_t visitor_bound(const sdpa_bwd_params* p)
+// Most kv-tiles that can visit one q-tile. The clamped q-tile ranges of
+// consecutive kv-tiles shift by one q-tile, so a q-tile has at most as many
+// visitors as a range is wide: 1 + ceil(W_left / 128) + ceil(W_right / 128),
+// plus one when the bottom-right diagonal shift is not a multiple of 128 or is
+// not known on the host (length arrays, packed sequences); every kv-tile when
+// the window is unbounded on either side.
+int64_t max_visitors(const sdpa_bwd_params* p)
 {
     const int64_t nkv = (p->s_kv + swa::kTileKV - 1) / swa::kTileKV;
     const int64_t right = p->mask_mode == SDPA_MASK_NONE ? p->window_right
                                                           : (p->window_right > 0 ? p->window_right : 0);
     if (p->window_left < 0 || right < 0) return nkv;
-    const int64_t span = swa::kTileQ + p->window_left + right;
-    const int64_t b = (span + swa::kTileKV - 1) / swa::kTileKV + 1;
-    return b < nkv ? b : nkv;
+    int64_t v = 1 + (p->window_left + swa::kTileQ - 1) / swa::kTileQ + (right + swa::kTileQ - 1) / swa::kTileQ;
+    if (p->mask_mode == SDPA_MASK_BOTTOM_RIGHT) {
+        const bool known = p->layout == SDPA_BSHD && p->seq_q_lens == nullptr && p->seq_kv_lens == nullptr;
+        if (!known || (p->s_kv - p->s_q) % swa::kTileKV != 0) ++v;
+    }
+    return v < nkv ? v : nkv;
 }
+
+// Strip mode of the main kernel (d = 64, at most two visitors per q-tile): the
+// two visitors of a q-tile combine dQ inside one CTA, or by arrival order
+// between two, without the relay or per-visitor slots.
+bool strip_mode(const sdpa_bwd_params* p) { return p->d == 64 && max_visitors(p) <= 2; }
 
 // Most workspace the per-visitor dQ slots may take; beyond it deterministic
 // mode keeps the relay.
@@ -162,8 +173,8 @@ swa::WsLayout layout_of(const sdpa_bwd_params* p)
     // instead of passing one tile along the relay, when the slots fit the cap.
     w.dq_part = off;
     w.n_slots = 0;
-    if (p->deterministic == 1) {
-        const int64_t bound = visitor_bound(p);
+    if (p->deterministic == 1 && !strip_mode(p)) {
+        const int64_t bound = max_visitors(p);
         const size_t bytes = static_cast<size_t>(p->b) * p->h_q * nqt * bound * swa::kTileQ * p->d * 4;
         if (bound >= 3 && bytes <= kSlotCapBytes) {
             w.n_slots = bound;
@@ -390,7 +401,7 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
     a.n_row_blocks = w.n_row_blocks;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (a.n_row_blocks == 0) {
-        // nothing to reduce: still reset status, ticket and the dSink output
+        // nothing to reduce: still reset the status words and the dSink output
         st = cuda_status(cudaMemsetAsync(a.status, 0, 8, s), "preprocess memset");
         if (st == SDPA_OK && p->dsink)
             st = cuda_status(cudaMemsetAsync(p->dsink, 0, p->h_q * sizeof(float), s), "dsink memset");
@@ -485,6 +496,7 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
         a.tm_part = a.tm_k;
     }
     a.items = at<uint8_t>(ws, w.items);
+    a.strip = strip_mode(p) ? 1 : 0;
     return cuda_status(swa::launch_main(a, p->dtype, static_cast<cudaStream_t>(stream)), "main launch");
 }
 
@@ -529,7 +541,11 @@ sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
     if (st != SDPA_OK) return st;
     st = cuda_status(cudaMemcpy(host, ws, sizeof(host), cudaMemcpyDeviceToHost), "status read");
     if (st != SDPA_OK) return st;
-    if (host[0] == SDPA_ERR_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a relay or MMA wait ran out on the device");
+    if (host[0] == SDPA_ERR_TIMEOUT)
+        return fail(SDPA_ERR_TIMEOUT, "a device wait ran out (%s)",
+                    host[1] == swa::kWhereRelay  ? "a dQ relay turn"
+                    : host[1] == swa::kWherePair ? "the partial of a dQ pair split between two CTAs"
+                                                 : "a hand-off inside the main kernel");
     if (host[0] == SDPA_ERR_BAD_LENGTHS)
         return fail(SDPA_ERR_BAD_LENGTHS, "a sequence length exceeds its slot (or s_q/s_kv)");
     if (host[0] == SDPA_ERR_UNSUPPORTED)

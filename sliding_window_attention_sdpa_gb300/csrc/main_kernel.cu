@@ -254,6 +254,21 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool v)
     return r != 0;
 }
 
+// Barrier over `count` threads (named barrier `id`) returning the OR of `v`.
+__device__ __forceinline__ bool bar_or(int id, int count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Optional timeline trace (build with -DSDPA_BWD_TRACE): SM clock stamps of each
 // role's hand-offs for the first kTraceCtas CTAs and kTraceTiles q-tiles, written
 // to the workspace at byte offset kTraceOffset (the caller sizes the workspace
@@ -279,12 +294,23 @@ struct Item {
     int64_t nq, steps;   // q-tiles per head, steps = group * nq
     bool has_work;       // at least one q-tile to sweep
     bool in_slot;        // the kv-tile has rows inside the sequence's slot
-    // Steps run q-head h0 .. h0 + group - 1, each over q-tiles q_hi - 1 down to
-    // q_lo; counters rather than divisions (there is no 64-bit divider, and
-    // these sit on every role's hand-off path).
+    // Steps run q-head h0 .. h0 + group - 1, each over its q-tiles from q_hi - 1
+    // down to q_lo, or (strip mode, UP) from q_lo up to q_hi - 1; counters
+    // rather than divisions (there is no 64-bit divider, and these sit on every
+    // role's hand-off path).
+    template <bool UP>
+    __device__ __forceinline__ int64_t first_j() const { return UP ? q_lo : q_hi - 1; }
+    template <bool UP>
     __device__ __forceinline__ void advance(int64_t& j, int64_t& hh) const
     {
-        if (j == q_lo) {
+        if constexpr (UP) {
+            if (j == q_hi - 1) {
+                j = q_lo;
+                ++hh;
+            } else {
+                ++j;
+            }
+        } else if (j == q_lo) {
             j = q_hi - 1;
             ++hh;
         } else {
@@ -308,24 +334,56 @@ struct Epi {
 // Per-launch constants of the item numbering (32-bit: the host keeps the item
 // count below 2^31).
 struct ItemCounts {
-    uint32_t h_kv, n_kv_tiles, group;
+    uint32_t h_kv, n_kv_tiles, group, b;
 };
 
+// The work items a CTA walks: begin, begin + stride, ... below end.
+//  - Round-robin (STRIP false): items numbered head-fastest, CTA c takes
+//    c, c + grid, ... The CTAs running at one time then cover all kv-heads of
+//    a few kv-tiles; in the [row][head][d] tensors one head is a narrow column
+//    of every row, so numbering them kv-tile fastest under this walk (all CTAs
+//    on one head) concentrates their loads and stores on a few memory
+//    partitions. The previous kv-tile of the same head (the dQ relay partner)
+//    is item - h_kv, which runs in the same wave.
+//  - Strip mode: items numbered (kv-head, sequence, kv-tile), kv-tile
+//    fastest; the grid is R CTAs per kv-head and CTA c walks kv-head c % h_kv
+//    over the (c / h_kv)-th of R equal contiguous runs of that head's
+//    (sequence, kv-tile) items, so that the two kv-tiles visiting a q-tile are
+//    consecutive items of one CTA except where a run ends. The CTAs on one run
+//    index read the same token rows of every head at about the same time, as
+//    the round-robin walk does.
+struct Walk {
+    int64_t begin, end, stride;
+};
+
+template <bool STRIP>
+__device__ __forceinline__ Walk item_walk(int64_t n_items, int64_t h_kv)
+{
+    if constexpr (STRIP) {
+        const int64_t runs = gridDim.x / h_kv, g = blockIdx.x % h_kv, run = blockIdx.x / h_kv;
+        const int64_t per_head = n_items / h_kv;
+        return Walk{g * per_head + per_head * run / runs, g * per_head + per_head * (run + 1) / runs, 1};
+    }
+    return Walk{static_cast<int64_t>(blockIdx.x), n_items, static_cast<int64_t>(gridDim.x)};
+}
+
+template <bool STRIP>
 __device__ __forceinline__ Item decode(const MainArgs& a, const ItemCounts& n, int64_t item)
 {
     const Geometry& g = a.g;
     Item it;
-    // Head-fastest numbering: the CTAs running at one time cover all kv-heads
-    // of a few kv-tiles. In the [row][head][d] tensors one head is a narrow
-    // column of every row, so kv-tile-fastest numbering (all CTAs on one head)
-    // concentrates their loads and stores on a few memory partitions. The
-    // previous kv-tile of the same head (the dQ relay partner) is then item
-    // - h_kv, which runs in the same wave.
     const uint32_t u = static_cast<uint32_t>(item);
-    const uint32_t rest = u / n.h_kv, bq = rest / n.n_kv_tiles;
-    it.gk = u - rest * n.h_kv;
-    it.t = rest - bq * n.n_kv_tiles;
-    it.bi = bq;
+    if constexpr (STRIP) {
+        const uint32_t rest = u / n.n_kv_tiles, gq = rest / n.b;
+        it.t = u - rest * n.n_kv_tiles;
+        it.bi = rest - gq * n.b;
+        it.gk = gq;
+    } else {
+        const uint32_t rest = u / n.h_kv, bq = rest / n.n_kv_tiles;
+        it.gk = u - rest * n.h_kv;
+        it.t = rest - bq * n.n_kv_tiles;
+        it.bi = bq;
+    }
     it.group = n.group;
     it.h0 = it.gk * it.group;
     it.s = seq_info(g, it.bi);
@@ -336,6 +394,27 @@ __device__ __forceinline__ Item decode(const MainArgs& a, const ItemCounts& n, i
     it.in_slot = it.kv_base < it.s.slot_kv;
     it.has_work = it.nq > 0 && it.in_slot;
     return it;
+}
+
+// Strip mode with one q-head per kv-head: a q-tile visited by kv-tiles t and
+// t + 1 that are consecutive items of this CTA is the last step of t and the
+// first of t + 1, so the second dQ contraction accumulates onto the first in
+// tensor memory and only the sum is read. Returns 1 for the first of such a
+// pair (its dQ is not read), 2 for the second (it reads the sum), else 0.
+template <bool STRIP>
+__device__ __forceinline__ int tmem_pair(const Geometry& g, const Item& it, int64_t j, int64_t item, const Walk& wk)
+{
+    if constexpr (!STRIP) {
+        return 0;
+    } else {
+        if (it.group != 1) return 0;
+        int64_t first, nvis;
+        q_tile_visitors(g, it.s, j, first, nvis);
+        if (nvis != 2) return 0;
+        const int turn = static_cast<int>(it.t - first);
+        const bool local = turn == 0 ? item + 1 < wk.end : item > wk.begin;
+        return local ? 1 + turn : 0;
+    }
 }
 
 // Zeroes rows [nvalid, 128) of a swizzled tile (whole 128-byte rows, so the
@@ -359,7 +438,17 @@ __device__ __forceinline__ void zero_tail(uint8_t* tile, int64_t nvalid, int lan
 
 }  // namespace
 
-template <int HD, bool BF16>
+// A global-memory wait (relay turn, split pair) that ran out: marks the CTA
+// aborted and records the status and which wait it was (out of line: cold).
+__device__ __noinline__ bool gave_up(int32_t* status, volatile uint32_t* abort_flag, int where)
+{
+    *abort_flag = 1;
+    set_status(status, kStatusTimeout);
+    set_status(status + 1, where);
+    return false;
+}
+
+template <int HD, bool BF16, bool STRIP>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a)
 {
     using C = Cfg<HD>;
@@ -384,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const int64_t n_items = g.b * g.h_kv * a.n_kv_tiles;
     const bool thd = g.layout == 1;
     const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
-                         static_cast<uint32_t>(g.h_q / g.h_kv)};
+                         static_cast<uint32_t>(g.h_q / g.h_kv), static_cast<uint32_t>(g.b)};
+    const Walk wk = item_walk<STRIP>(n_items, g.h_kv);
 
     if (tid == 0) {
         misc[1] = 0;
@@ -421,10 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     Item* items = static_cast<Item*>(a.items);
     const bool use_items = C::kAhead && a.use_items != 0;
     if (use_items)
-        for (int64_t item = blockIdx.x + static_cast<int64_t>(tid) * gridDim.x; item < n_items;
-             item += static_cast<int64_t>(kThreads) * gridDim.x)
-            items[item] = decode(a, cnt, item);
-    auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode(a, cnt, i); };
+        for (int64_t item = wk.begin + static_cast<int64_t>(tid) * wk.stride; item < wk.end;
+             item += static_cast<int64_t>(kThreads) * wk.stride)
+            items[item] = decode<STRIP>(a, cnt, item);
+    auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode<STRIP>(a, cnt, i); };
     tc_fence_before();
     __syncthreads();   // also publishes the item table to the CTA
     tc_fence_after();
@@ -451,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
-            for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+            for (int64_t item = wk.begin; item < wk.end; item += wk.stride) {
                 const Item it = item_at(item);
                 if (use_items) {
                     // The next two items' records toward this SM's L1, ahead of
                     // the roles' reads (every role reaches them after this warp).
-                    for (int64_t nx = item + gridDim.x; nx < n_items && nx <= item + 2 * gridDim.x; nx += gridDim.x) {
+                    for (int64_t nx = item + wk.stride; nx < wk.end && nx <= item + 2 * wk.stride; nx += wk.stride) {
                         const char* rec = reinterpret_cast<const char*>(items + nx);
                         prefetch_l1(rec);
                         prefetch_l1(rec + kItemBytes / 2);
@@ -474,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 tma_tile<HD>(sbase + C::kV + ks * C::kTile, &a.tm_v, bar(kKvFull0 + ks), thd,
                              (int)it.gk, kvrow, (int)it.bi);
                 bool ok = true;
-                for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
+                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
                     SWA_TRACE(12, q_it);
@@ -507,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             bool valid, first, last;  // first / last step of its work item
             int st, ks;               // Q/dO and K/V ring entries
             uint32_t q_it;            // step index (selects the dS^T buffer)
+            int tpair;                // tmem_pair() of the step
         };
-        Pending pend{false, false, false, 0, 0, 0u};
+        Pending pend{false, false, false, 0, 0, 0u, 0};
         // dV += P^T dO, dK += dS^T Q, dQ = dS K for step `p` (softmax done).
         auto issue_grads = [&](const Pending& p) -> bool {
             if (p.first && !wait_warp(kAccEmpty, (acc_it & 1) ^ 1)) return false;
@@ -548,16 +639,20 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             }
             __syncwarp();
             // dQ overwrites the TMEM columns the dQ warps read for the last step;
-            // waiting only here lets dV and dK run meanwhile
-            if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
-            ++dq_it;
+            // waiting only here lets dV and dK run meanwhile. The second step of
+            // a tensor-memory pair adds onto the first's (unread) dQ instead.
+            const bool dq_onto = p.tpair == 2;
+            if (!dq_onto) {
+                if (!C::kDqAliasesS && !wait_warp(kDqEmpty, (dq_it & 1) ^ 1)) return false;
+                ++dq_it;
+            }
             {
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ, k > 0);
-                umma_commit(bar(kDqFull));
+                    umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ, k > 0 || dq_onto);
+                if (p.tpair != 1) umma_commit(bar(kDqFull));
                 SWA_TRACE(4, p.q_it);
                 if (p.last) {
                     // after dQ: the epilogue stages dK/dV in this step's dS^T buffer
@@ -570,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             return true;
         };
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int64_t item = wk.begin; item < wk.end && ok; item += wk.stride) {
             const Item it = item_at(item);
             if (!it.has_work) continue;
             const int ks = kv_it % C::kKvStages;
@@ -579,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             const uint32_t sK = sbase + C::kK + ks * C::kTile, sV = sbase + C::kV + ks * C::kTile;
             if (it.kv_base + kTileKV > it.s.len_kv)
                 zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
-            for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
+            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
                 const int st = q_it % C::kStages;
                 if (!(ok = wait_warp(kQFull0 + st, (q_it / C::kStages) & 1))) break;
                 if (lane == 0) SWA_TRACE(0, q_it);
@@ -616,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     SWA_TRACE(1, q_it);
                 }
                 __syncwarp();
-                const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it};
+                const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it, tmem_pair<STRIP>(g, it, j, item, wk)};
                 if constexpr (C::kAhead) {
                     if (pend.valid && !(ok = issue_grads(pend))) break;
                     pend = cur;
@@ -730,11 +825,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         // The next item's record is read right after this one's last P^T
         // hand-off, so that the load overlaps the epilogue bookkeeping.
-        auto decode_at = [&](int64_t i) -> Item { return item_at(i < n_items ? i : blockIdx.x); };
-        Item it = item_at(blockIdx.x), nxt;
+        auto decode_at = [&](int64_t i) -> Item { return item_at(i < wk.end ? i : wk.begin); };
+        Item it = item_at(wk.begin), nxt;
         bool have_nxt = false;
-        for (int64_t item = blockIdx.x; item < n_items;
-             item += gridDim.x, it = have_nxt ? nxt : decode_at(item), have_nxt = false) {
+        for (int64_t item = wk.begin; item < wk.end;
+             item += wk.stride, it = have_nxt ? nxt : decode_at(item), have_nxt = false) {
             const int64_t kj = it.kv_base + r;
             if (r == 0 && half == 0 && it.s.bad && it.t == 0 && it.gk == 0)
                 set_status(a.status, kStatusBadLengths);
@@ -743,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - it.s.diag);
                 if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - it.s.diag);
                 if (kj >= it.s.len_kv) i_hi = -1;
-                for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, ++q_it, it.advance(j, hh)) {
+                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(20, q_it);
                     release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
@@ -848,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         run_epi(*epi_slot);
                     }
                 }
-                nxt = decode_at(item + gridDim.x);
+                nxt = decode_at(item + wk.stride);
                 have_nxt = true;
             }
             if (!it.in_slot) continue;
@@ -892,31 +987,49 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const uint32_t stg_s = sbase + C::kDqStage;
         uint32_t dq_it = 0, ld_it = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int64_t item = wk.begin; item < wk.end && ok; item += wk.stride) {
             const Item it = item_at(item);
             if (!it.has_work) continue;
-            for (int64_t k = 0, j = it.q_hi - 1, hh = it.h0; k < it.steps; ++k, it.advance(j, hh)) {
+            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, it.template advance<STRIP>(j, hh)) {
                 // this visit's bookkeeping first, while the dQ contraction runs
                 // (after the wait it delayed the TMEM read by ~1 K cycles)
                 int64_t first, nvis;
                 q_tile_visitors(g, it.s, j, first, nvis);
                 const int turn = static_cast<int>(it.t - first);
-                const bool single = nvis <= 1;
                 int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
-                // two visitors, or deterministic mode where no per-visitor slots
-                // apply (fewer than three visitors, or none allotted): hand the
-                // tile along in turn order
-                const bool relay = nvis == 2 || (a.deterministic && (nvis < 3 || a.n_slots == 0));
-                // deterministic mode otherwise: each visitor stores its own fp32
-                // partial (slot = turn), which the convert kernel sums in visitor
-                // order
-                const bool slots = a.deterministic && !relay;
-                const bool conv_now = single || (relay && turn == nvis - 1);
-                // accumulator write: a store for the first relay turn, else an add
-                const bool add = !(relay && turn == 0);
                 // TMA writes whole 128-row boxes: the tile must lie inside the
                 // sequence's slot (always so for BSHD, whose maps end at s_q)
                 const bool use_tma = !thd || (j + 1) * kTileQ <= it.s.slot_q;
+                // Strip mode (at most two visitors, kv-tiles t and t + 1 of one
+                // head): the two are consecutive items of this CTA unless its run
+                // ends between them ("local"), and combine with no waiting. With
+                // one q-head per kv-head their dQ contractions add up in tensor
+                // memory; otherwise the first stores its fp32 partial in the
+                // accumulator rows and the second loads it back. A pair split
+                // between two CTAs goes by arrival order: the first to arrive
+                // stores its partial and flags it, the second adds it to its own.
+                // A sum of two rounded partials does not depend on their order,
+                // so this stays bitwise repeatable.
+                const bool local = STRIP && nvis == 2 && (turn == 0 ? item + 1 < wk.end : item > wk.begin);
+                // one q-head per kv-head: the pair's dQ adds up in tensor memory
+                // (tmem_pair); the first step reads nothing, the second the sum
+                const int tpair = local && it.group == 1 ? 1 + turn : 0;
+                if (tpair == 1) continue;
+                const bool pair = STRIP && nvis == 2 && !local;
+                const bool single = nvis <= 1 || tpair == 2;   // no partial to combine
+                // two visitors, or deterministic mode where no per-visitor slots
+                // apply (fewer than three visitors, or none allotted): hand the
+                // tile along in turn order
+                const bool relay = !STRIP && (nvis == 2 || (a.deterministic && (nvis < 3 || a.n_slots == 0)));
+                // deterministic mode otherwise: each visitor stores its own fp32
+                // partial (slot = turn), which the convert kernel sums in visitor
+                // order
+                const bool slots = !STRIP && a.deterministic && !relay;
+                bool conv_now = single || (relay && turn == nvis - 1) || (local && turn == 1);
+                const bool lpair = local && !tpair;   // a local pair through the accumulator rows
+                // accumulator write: a store for the first relay turn (and for
+                // every strip-mode partial), else an add
+                const bool add = !STRIP && !(relay && turn == 0);
                 const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
                 const int tb = static_cast<int>(it.bi), th = static_cast<int>(hh);
                 if (r == 0) bulk_wait_read0();   // the staging is free again
@@ -926,23 +1039,42 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 tc_fence_after();
                 // Waits for this visit's turn (relay) in thread 0; true in all 128
                 // threads if the turn came (or none was needed) and nothing aborted.
+                bool early = false;   // pair: this visitor arrived first
                 auto wait_turn = [&]() -> bool {
                     bool mine = true;
+                    if (pair && r == 0) {
+                        // each arrival adds 1; the first adds 4 once its partial
+                        // is in place, which the second waits for
+                        early = atom_add_acq_rel_gpu(sem, 1) == 0;
+                        if (!early) {
+                            const uint64_t t0 = globaltimer_ns();
+                            while (!(ld_acquire_gpu(sem) & 4)) {
+                                if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+                                    mine = gave_up(a.status, abort_flag, kWherePair);
+                                    break;
+                                }
+                            }
+                            fence_proxy_async_global();
+                        }
+                    }
                     if (relay && turn > 0 && r == 0) {
                         const uint64_t t0 = globaltimer_ns();
                         for (;;) {
                             if (ld_acquire_gpu(sem) == turn) break;
                             if (*abort_flag || globaltimer_ns() - t0 > tmo) {
-                                set_status(a.status, kStatusTimeout);
-                                *abort_flag = 1;
-                                mine = false;
+                                mine = gave_up(a.status, abort_flag, kWhereRelay);
                                 break;
                             }
                         }
                         // later async-proxy writes follow the acquired ones
                         fence_proxy_async_global();
                     }
-                    return bar_and(kBarDq, 128, mine && *abort_flag == 0);
+                    const bool go_on = bar_and(kBarDq, 128, mine && *abort_flag == 0);
+                    if (pair) {
+                        early = bar_or(kBarDq, 128, early);   // thread 0's arrival, to the group
+                        conv_now = !early;
+                    }
+                    return go_on;
                 };
                 // Converts 32 dQ values of this row (columns [32 ch, 32 ch + 32)),
                 // adding the earlier visitors' partial sum unless alone, into the
@@ -1068,6 +1200,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             // fp32 tile into the staging; each thread then adds its
                             // row and writes it back converted, in place
                             if (r == 0) {
+                                if (lpair) {
+                                    // this thread stored the partial in an earlier step
+                                    bulk_wait0();
+                                    fence_proxy_async_global();
+                                }
                                 mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
                                 tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
                                 tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
@@ -1082,6 +1219,17 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                     const float4 x0 = *reinterpret_cast<const float4*>(stg + stg_off(r, 2 * i));
                                     const float4 x1 = *reinterpret_cast<const float4*>(stg + stg_off(r, 2 * i + 1));
                                     const uint32_t* v = i < 4 ? v0 + 8 * i : v1 + 8 * (i - 4);
+                                    if constexpr (STRIP) {
+                                        // own partial rounded, then one add: a two-term
+                                        // sum that does not depend on which came first
+                                        auto sum = [&](int e, float x) {
+                                            return __fadd_rn(__fmul_rn(__uint_as_float(v[e]), a.scale), x);
+                                        };
+                                        *reinterpret_cast<uint4*>(stg + stg_off(r, i)) = make_uint4(
+                                            pack2<BF16>(sum(0, x0.x), sum(1, x0.y)), pack2<BF16>(sum(2, x0.z), sum(3, x0.w)),
+                                            pack2<BF16>(sum(4, x1.x), sum(5, x1.y)), pack2<BF16>(sum(6, x1.z), sum(7, x1.w)));
+                                        continue;
+                                    }
                                     *reinterpret_cast<uint4*>(stg + stg_off(r, i)) = make_uint4(
                                         pack2<BF16>(fmaf(__uint_as_float(v[0]), a.scale, x0.x),
                                                     fmaf(__uint_as_float(v[1]), a.scale, x0.y)),
@@ -1179,6 +1327,23 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     }
                 }
                 if (r == 0) SWA_TRACE(11, dq_it - 1);
+                if (pair && early && go) {
+                    // the partial is in place: complete its copies, then flag it (+4)
+                    if (use_tma) {
+                        if (r == 0) {
+                            bulk_wait0();
+                            fence_proxy_async_global();
+                            red_add_release_gpu(sem, 4);
+                        }
+                    } else {
+                        named_bar_sync(kBarDq, 128);
+                        if (r == 0) {
+                            __threadfence();
+                            red_add_release_gpu(sem, 4);
+                        }
+                    }
+                    continue;
+                }
                 if (!relay || turn + 1 >= nvis) continue;
                 // publish this turn's partial sum to the next visitor
                 if (use_tma) {
@@ -1206,10 +1371,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     }
 }
 
-template <int HD, bool BF16>
+template <int HD, bool BF16, bool STRIP>
 static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 {
-    auto kern = sdpa_bwd_main_kernel<HD, BF16>;
+    auto kern = sdpa_bwd_main_kernel<HD, BF16, STRIP>;
     const uint32_t bytes = Cfg<HD>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
@@ -1218,7 +1383,15 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t grid = items < sms ? items : sms;
+    int64_t grid = items < sms ? items : sms;
+    if constexpr (STRIP) {
+        // R runs per kv-head, at least one item each (the host falls back to
+        // the round-robin walk when there are more kv-heads than SMs)
+        const int64_t per_head = items / a.g.h_kv;
+        int64_t runs = sms / a.g.h_kv;
+        if (runs > per_head) runs = per_head;
+        grid = runs * a.g.h_kv;
+    }
     MainArgs b = a;
     b.use_items = items <= kItemTableMaxPerCta * grid;
     kern<<<static_cast<unsigned>(grid), kThreads, bytes, s>>>(b);
@@ -1227,8 +1400,11 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 
 cudaError_t launch_main(const MainArgs& a, int dtype, cudaStream_t s)
 {
-    if (a.g.d == 64) return dtype == 0 ? launch_typed<64, true>(a, s) : launch_typed<64, false>(a, s);
-    return dtype == 0 ? launch_typed<128, true>(a, s) : launch_typed<128, false>(a, s);
+    if (a.g.d == 64) {
+        if (a.strip) return dtype == 0 ? launch_typed<64, true, true>(a, s) : launch_typed<64, false, true>(a, s);
+        return dtype == 0 ? launch_typed<64, true, false>(a, s) : launch_typed<64, false, false>(a, s);
+    }
+    return dtype == 0 ? launch_typed<128, true, false>(a, s) : launch_typed<128, false, false>(a, s);
 }
 
 }  // namespace swa

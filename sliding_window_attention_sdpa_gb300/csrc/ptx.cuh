@@ -318,6 +318,11 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p)
     return v;
 }
 
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_release_gpu(int* p, int v)
 {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

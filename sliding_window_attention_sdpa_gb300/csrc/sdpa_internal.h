@@ -32,10 +32,14 @@ constexpr size_t kItemBytes = 152;
 constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;
+// Second status word: which global-memory wait of the main kernel ran out
+// first (0: none, or an mbarrier hand-off inside a CTA).
+constexpr int kWhereRelay = 200;   // a relay turn
+constexpr int kWherePair = 201;    // the partial of a strip-mode pair split between two CTAs
 
 // Workspace layout (byte offsets from the workspace base, 256-B aligned).
 struct WsLayout {
-    size_t status;      // int32 status, int32 ticket counter
+    size_t status;      // int32 status, int32 where (which global-memory wait ran out)
     size_t dq_acc;      // fp32 [rows_q][h_q][d]
     size_t stats;       // fp32 per-row statistics, [b][h_q][n_q_tiles][2][128]: per q-tile
                         // 128 x -LSE * log2(e), then 128 x -D
@@ -86,7 +90,7 @@ struct PreArgs {
     // with one packed fp32x2 FMA and each pair of (dP - D) with one packed add.
     float* stats;
     int64_t stats_row;   // rows per (sequence, q-head): n_q_tiles * 128 (2 floats each)
-    int32_t* status;     // status + ticket (2 ints)
+    int32_t* status;     // status + where (2 ints)
     int32_t* sems;
     int64_t n_sems;
     float* dsink_part;
@@ -128,6 +132,12 @@ struct MainArgs {
     // items; with many, the roles decode in place)
     void* items;
     int32_t use_items;
+    // Strip mode (the launcher sets it when no q-tile can have more than two
+    // visiting kv-tiles, d = 64): each CTA walks a contiguous run of work items
+    // numbered kv-tile fastest and sweeps each item's q-tiles from the bottom
+    // up, so that the two visitors of a q-tile are consecutive steps of one CTA
+    // except where the run ends.
+    int32_t strip;
 };
 
 struct CvtArgs {

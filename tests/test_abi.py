@@ -71,12 +71,16 @@ def test_deterministic_slots_workspace():
     # 4 kv-tiles may visit each of the 4 q-tiles
     extra = p.b * p.h_q * 4 * 4 * 128 * p.d * 4
     assert base + extra <= slots <= base + extra + 256
-    # W = 32 over 4 kv-tiles: up to three kv-tiles may reach a q-tile's rows
-    s512 = dict(s_q=512, s_kv=512)
+    # W = 200 over 4 kv-tiles: a q-tile's rows reach back 200 keys, so up to
+    # 1 + ceil(200 / 128) = 3 kv-tiles visit it
+    s512 = dict(s_q=512, s_kv=512, window_left=200)
     assert (swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1, **s512))
             > swa.sdpa_bwd_workspace_bytes(base_params(**s512)))
-    # ... but only two of the 2 kv-tiles of 256 rows; no slots
-    assert swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1)) == swa.sdpa_bwd_workspace_bytes(base_params())
+    # W = 32: at most 1 + ceil(32 / 128) = 2 visitors (the strip-mode kernel
+    # combines them without slots), at either length
+    for extra_kw in (dict(s_q=512, s_kv=512), {}):
+        assert (swa.sdpa_bwd_workspace_bytes(base_params(deterministic=1, **extra_kw))
+                == swa.sdpa_bwd_workspace_bytes(base_params(**extra_kw)))
 
 
 def test_workspace_bytes():
