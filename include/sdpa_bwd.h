@@ -184,8 +184,10 @@ sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace
 
 /*
  * Synchronises `stream` and returns the device status word of the last
- * backward run on `workspace`: SDPA_OK, SDPA_ERR_TIMEOUT (a relay wait gave up;
- * dQ is then incomplete), SDPA_ERR_BAD_LENGTHS, or SDPA_ERR_UNSUPPORTED (the
+ * backward run on `workspace`: SDPA_OK, SDPA_ERR_TIMEOUT (a device wait gave
+ * up -- a dQ relay turn, the partial of a dQ pair split between two CTAs, or a
+ * hand-off inside the main kernel, named by sdpa_bwd_last_error(); the
+ * gradients are then incomplete), SDPA_ERR_BAD_LENGTHS, or SDPA_ERR_UNSUPPORTED (the
  * device placed the main kernel's dynamic shared memory off a 1024-byte
  * boundary, which its swizzled tiles need; it then computed nothing).
  */
@@ -225,6 +227,24 @@ sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params *params, void *stream);
 
 /* Message of the last host-side error on the calling thread ("" if none). */
 const char *sdpa_bwd_last_error(void);
+
+/*
+ * Test hook for the device-side failure handling; not for production use.
+ * Every wait inside the backward kernels is bounded (2 s by default): a wait
+ * that runs out records SDPA_ERR_TIMEOUT in the workspace's status word, the
+ * kernel stops issuing work, lets the copies and contractions already in
+ * flight finish, frees its tensor memory and returns, and
+ * sdpa_bwd_check_status() reports it (the gradients are then incomplete).
+ * This call changes, for the calling thread's later sdpa_bwd() calls:
+ *   wait_limit_ns  the bound of every device wait (<= 0: the default);
+ *   flags          bit 0: each dQ relay turn waits for a counter value no
+ *                  visitor writes; bit 1: the second visitor of a dQ pair split
+ *                  between two CTAs waits for a flag no visitor sets (both
+ *                  waits then run out); 0: normal operation.
+ * Returns SDPA_ERR_INVALID_ARG for undefined flag bits. Call it with (0, 0) to
+ * restore normal operation.
+ */
+sdpa_status_t sdpa_bwd_test_hook(int64_t wait_limit_ns, int32_t flags);
 
 /* sizeof(sdpa_bwd_params) as compiled into the library, for binding checks. */
 size_t sdpa_bwd_params_bytes(void);

@@ -29,7 +29,8 @@ ENTRY_POINTS = ("sdpa_bwd_workspace_bytes", "sdpa_bwd_preprocess", "sdpa_bwd",
                 "sdpa_bwd_dq_convert", "sdpa_bwd_gqa_reduce", "sdpa_bwd_check_status",
                 "sdpa_bwd_last_error", "sdpa_bwd_params_bytes", "sdpa_bwd_tile_kv",
                 "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc", "sdpa_bwd_kernel_launches",
-                "sdpa_fwd", "sdpa_fwd_check_status", "sdpa_fwd_params_bytes")
+                "sdpa_fwd", "sdpa_fwd_check_status", "sdpa_fwd_params_bytes",
+                "sdpa_bwd_test_hook")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -118,6 +119,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.sdpa_bwd_tile_q.restype = ctypes.c_int32
         lib.sdpa_bwd_kernel_launches.argtypes = [P]
         lib.sdpa_bwd_kernel_launches.restype = ctypes.c_int32
+        lib.sdpa_bwd_test_hook.argtypes = [ctypes.c_int64, ctypes.c_int32]
+        lib.sdpa_bwd_test_hook.restype = st
         lib.sdpa_fwd.argtypes = [ctypes.POINTER(SdpaFwdParams), vp]
         lib.sdpa_fwd.restype = st
         lib.sdpa_fwd_check_status.argtypes = [vp]
@@ -175,6 +178,12 @@ def sdpa_bwd_check_status(workspace: int, stream: int) -> int:
 
 # Largest scratch (bytes) sdpa_bwd_no_alloc can serve; see include/sdpa_bwd.h.
 SDPA_BWD_NO_ALLOC_MAX_BYTES = 32 << 20
+
+
+def sdpa_bwd_test_hook(wait_limit_ns: int, flags: int) -> int:
+    """Test-only: device wait limit and unreachable-wait flags for this
+    thread's later sdpa_bwd calls (see the C header); (0, 0) restores them."""
+    return load().sdpa_bwd_test_hook(int(wait_limit_ns), int(flags))
 
 
 def sdpa_bwd_no_alloc(params, stream: int) -> int:

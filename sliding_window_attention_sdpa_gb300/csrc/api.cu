@@ -20,6 +20,11 @@ namespace {
 
 thread_local std::string g_last_error;
 
+// sdpa_bwd_test_hook's settings for this thread's next sdpa_bwd calls.
+constexpr int64_t kWaitLimitNs = 2000000000LL;
+thread_local int64_t g_test_wait_ns = 0;
+thread_local int32_t g_test_flags = 0;
+
 sdpa_status_t fail(sdpa_status_t code, const char* fmt, ...)
 {
     char buf[512];
@@ -451,7 +456,8 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     a.scale = p->scale;
     a.scale_log2 = p->scale * 1.4426950408889634f;
     a.deterministic = p->deterministic;
-    a.timeout_ns = 2000000000LL;
+    a.timeout_ns = g_test_wait_ns > 0 ? g_test_wait_ns : kWaitLimitNs;
+    a.test_flags = g_test_flags;
     if (p->b * p->h_q * a.n_kv_tiles == 0) return SDPA_OK;
     const bool thd = p->layout == SDPA_THD;
     const int64_t rq = thd ? p->total_q : p->s_q, rk = thd ? p->total_kv : p->s_kv;
@@ -555,6 +561,15 @@ sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
 }
 
 const char* sdpa_bwd_last_error(void) { return g_last_error.c_str(); }
+
+sdpa_status_t sdpa_bwd_test_hook(int64_t wait_limit_ns, int32_t flags)
+{
+    if (flags & ~3) return fail(SDPA_ERR_INVALID_ARG, "test hook flags=%d: only bits 0 and 1 are defined", flags);
+    g_test_wait_ns = wait_limit_ns > 0 ? wait_limit_ns : 0;
+    g_test_flags = flags;
+    g_last_error.clear();
+    return SDPA_OK;
+}
 
 }  // extern "C"
 
@@ -769,7 +784,7 @@ sdpa_status_t sdpa_fwd(const sdpa_fwd_params* f, void* stream)
     copy3(a.o_stride, f->o_stride);
     a.n_q_tiles = n_q_tiles;
     a.scale_log2 = f->scale * 1.4426950408889634f;
-    a.timeout_ns = 2000000000LL;
+    a.timeout_ns = kWaitLimitNs;
     // the maps' row extent is one sequence slot (BSHD: s, where a 4-D map
     // clips boxes that overhang it) or the packed tokens (THD)
     const int64_t rq_map = thd ? p.total_q : p.s_q, rk_map = thd ? p.total_kv : p.s_kv;

@@ -111,7 +111,7 @@ struct Cfg {
 // mbarrier indices
 enum Bar : int {
     kSFull = 0, kPFull, kPEmpty, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
-    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kDqLoad, kNumBars
+    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kDqLoad, kDrain, kNumBars
 };
 
 template <bool BF16>
@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         mbar_init(bar(kAccFull), 1);
         mbar_init(bar(kAccEmpty), kSoftThreads);
         mbar_init(bar(kDqLoad), 1);
+        mbar_init(bar(kDrain), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(kQFull0 + s), 1);
             mbar_init(bar(kQEmpty0 + s), 1);
@@ -582,6 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 }
                 if (!ok) break;
             }
+            // After a wait gave up, loads may still be on their way into this
+            // CTA's shared memory: wait (bounded) for the last one issued on each
+            // ring entry before the CTA can exit (at most one is outstanding per
+            // entry; one that the consumer saw complete returns at once).
+            for (uint32_t i = kv_it > C::kKvStages ? kv_it - C::kKvStages : 0; i < kv_it; ++i)
+                mbar_wait(bar(kKvFull0 + i % C::kKvStages), (i / C::kKvStages) & 1, tmo);
+            for (uint32_t i = q_it > C::kStages ? q_it - C::kStages : 0; i < q_it; ++i)
+                mbar_wait(bar(kQFull0 + i % C::kStages), (i / C::kStages) & 1, tmo);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -728,6 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             ++p_it;
             if (ok) issue_grads(pend);
         }
+        // every contraction issued has finished before TMEM is freed (after a
+        // wait gave up some may still be running)
+        umma_commit(bar(kDrain));
+        mbar_wait(bar(kDrain), 0, tmo);
     } else if (warp < kWarpSoft0) {
         // warps 2-3: no role
     } else if (warp < kWarpDq0) {
@@ -965,6 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             named_bar_sync(kBarSoft, kSoftThreads);   // epi_slot's write is visible
             run_epi(*epi_slot);
         }
+        if constexpr (C::kPInTmem) tmem_st_wait();   // a step left early may have P^T stores in flight
     } else {
         // ------------------------------------------------------------ dQ
         // Visitors of a q-tile are the contiguous kv-tiles [first, first + n).
@@ -1048,7 +1062,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         early = atom_add_acq_rel_gpu(sem, 1) == 0;
                         if (!early) {
                             const uint64_t t0 = globaltimer_ns();
-                            while (!(ld_acquire_gpu(sem) & 4)) {
+                            const int flag = (a.test_flags & 2) ? 1024 : 4;
+                            while (!(ld_acquire_gpu(sem) & flag)) {
                                 if (*abort_flag || globaltimer_ns() - t0 > tmo) {
                                     mine = gave_up(a.status, abort_flag, kWherePair);
                                     break;
@@ -1060,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (relay && turn > 0 && r == 0) {
                         const uint64_t t0 = globaltimer_ns();
                         for (;;) {
-                            if (ld_acquire_gpu(sem) == turn) break;
+                            if (ld_acquire_gpu(sem) == turn + ((a.test_flags & 1) << 30)) break;
                             if (*abort_flag || globaltimer_ns() - t0 > tmo) {
                                 mine = gave_up(a.status, abort_flag, kWhereRelay);
                                 break;
@@ -1360,6 +1375,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 }
             }
         }
+        // a partner tile whose load a given-up wait did not see complete
+        if (r == 0 && ld_it > 0) mbar_wait(bar(kDqLoad), (ld_it - 1) & 1, tmo);
     }
 
     bulk_wait0();   // copies issued from this CTA's shared memory are complete

@@ -138,6 +138,11 @@ struct MainArgs {
     // up, so that the two visitors of a q-tile are consecutive steps of one CTA
     // except where the run ends.
     int32_t strip;
+    // Test hook (zero in normal use): bit 0 makes every relay turn wait for a
+    // counter value no visitor writes, bit 1 makes the second arrival of a
+    // pair split between two CTAs wait for a flag no visitor sets; with a short
+    // timeout_ns both give up and report SDPA_ERR_TIMEOUT.
+    int32_t test_flags;
 };
 
 struct CvtArgs {
