@@ -212,18 +212,29 @@ sdpa_status_t sdpa_bwd_check_status(const void *workspace, void *stream);
  *    deterministic mode 1 the per-visitor dQ slots are dropped first (the call
  *    runs as mode 2, the relay: also bitwise repeatable) when that makes the
  *    problem fit.
- *  - Set-up: the first call on a device (with that device current) looks up
- *    the array's device address once; make that first call before any stream
+ *  - Set-up: every call looks up the array's device address on the current
+ *    device (cudaGetSymbolAddress: no allocation). The first call on a device
+ *    may load the library's device code there, so make it before any stream
  *    capture.
  *  - Sharing: every call on a device uses the same array and leaves its
  *    contents behind; each call re-zeroes what must start at zero. Calls whose
  *    work overlaps on the GPU (other streams, other threads) race on the array
  *    and must be serialised by the caller.
- *  - Device-side status (a relay wait that ran out) is not reported by this
- *    entry point; host-side errors are, as for the other calls.
+ *  - Device-side status (a wait that ran out, lengths longer than their
+ *    slots) lands at the start of the array: sdpa_bwd_no_alloc_check_status()
+ *    reads it. Host-side errors are returned as for the other calls.
  */
 #define SDPA_BWD_NO_ALLOC_MAX_BYTES ((size_t)32 << 20)
 sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params *params, void *stream);
+
+/*
+ * Device status of the last sdpa_bwd_no_alloc run on the current device, as
+ * sdpa_bwd_check_status() reports it for a workspace: synchronises `stream`
+ * (the stream that run was enqueued on) and reads the status word at the start
+ * of the fixed scratch. Like the array itself, the word is shared by every call
+ * on the device. Allocates nothing. The pages have no counterpart to this call.
+ */
+sdpa_status_t sdpa_bwd_no_alloc_check_status(void *stream);
 
 /* Message of the last host-side error on the calling thread ("" if none). */
 const char *sdpa_bwd_last_error(void);

@@ -21,7 +21,8 @@
  * Errors: host-side validation returns SDPA_ERR_INVALID_ARG / UNSUPPORTED with
  * a message (sdpa_bwd_last_error()); launch failures SDPA_ERR_CUDA. Every wait
  * inside the kernel is bounded; a wait that runs out sets a device status
- * word that sdpa_fwd_check_status() returns (SDPA_ERR_TIMEOUT).
+ * word, shared by all forwards on the device, that sdpa_fwd_check_status()
+ * returns (SDPA_ERR_TIMEOUT).
  */
 #ifndef SDPA_FWD_H
 #define SDPA_FWD_H
@@ -61,7 +62,13 @@ typedef struct sdpa_fwd_params {
 sdpa_status_t sdpa_fwd(const sdpa_fwd_params *params, void *stream);
 
 /* Synchronises `stream` and returns the forward's device status on the
- * current device (SDPA_OK or SDPA_ERR_TIMEOUT), then clears it. */
+ * current device (SDPA_OK or SDPA_ERR_TIMEOUT), then clears it.
+ * The status word is one per device, shared by every sdpa_fwd call on it (the
+ * forward takes no workspace): a timeout of any forward on the device is
+ * reported by the next check, whichever stream it ran on, and forwards that
+ * run concurrently on other streams while this call reads and clears the word
+ * may have their status cleared with it. Check from one stream at a time, or
+ * after synchronising the device, to attribute a status to one call. */
 sdpa_status_t sdpa_fwd_check_status(void *stream);
 
 /* sizeof(sdpa_fwd_params) as compiled into the library, for binding checks. */

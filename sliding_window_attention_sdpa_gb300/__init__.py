@@ -30,7 +30,7 @@ ENTRY_POINTS = ("sdpa_bwd_workspace_bytes", "sdpa_bwd_preprocess", "sdpa_bwd",
                 "sdpa_bwd_last_error", "sdpa_bwd_params_bytes", "sdpa_bwd_tile_kv",
                 "sdpa_bwd_tile_q", "sdpa_bwd_no_alloc", "sdpa_bwd_kernel_launches",
                 "sdpa_fwd", "sdpa_fwd_check_status", "sdpa_fwd_params_bytes",
-                "sdpa_bwd_test_hook")
+                "sdpa_bwd_test_hook", "sdpa_bwd_no_alloc_check_status")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -121,6 +121,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.sdpa_bwd_kernel_launches.restype = ctypes.c_int32
         lib.sdpa_bwd_test_hook.argtypes = [ctypes.c_int64, ctypes.c_int32]
         lib.sdpa_bwd_test_hook.restype = st
+        lib.sdpa_bwd_no_alloc_check_status.argtypes = [vp]
+        lib.sdpa_bwd_no_alloc_check_status.restype = st
         lib.sdpa_fwd.argtypes = [ctypes.POINTER(SdpaFwdParams), vp]
         lib.sdpa_fwd.restype = st
         lib.sdpa_fwd_check_status.argtypes = [vp]
@@ -178,6 +180,11 @@ def sdpa_bwd_check_status(workspace: int, stream: int) -> int:
 
 # Largest scratch (bytes) sdpa_bwd_no_alloc can serve; see include/sdpa_bwd.h.
 SDPA_BWD_NO_ALLOC_MAX_BYTES = 32 << 20
+
+
+def sdpa_bwd_no_alloc_check_status(stream: int) -> int:
+    """Device status of the last sdpa_bwd_no_alloc run on this device."""
+    return load().sdpa_bwd_no_alloc_check_status(stream)
 
 
 def sdpa_bwd_test_hook(wait_limit_ns: int, flags: int) -> int:

@@ -578,39 +578,22 @@ sdpa_status_t sdpa_bwd_test_hook(int64_t wait_limit_ns, int32_t flags)
 // allocate device memory (see sdpa_bwd_no_alloc in the header). Its scratch is
 // this fixed array; host code never uses the array's name as an address (on
 // the host it is only a stand-in): the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up on every call with the caller's device
+// current (cheap, allocates nothing, and never stale after a device reset).
 namespace {
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[SDPA_BWD_NO_ALLOC_MAX_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
-
 sdpa_status_t no_alloc_scratch(void** out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
-        return fail(SDPA_ERR_CUDA, "sdpa_bwd_no_alloc: no current CUDA device (%s)",
+        return fail(SDPA_ERR_CUDA, "sdpa_bwd_no_alloc: cannot resolve the scratch array on the current device (%s)",
                     cudaGetErrorString(e));
     }
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(SDPA_ERR_UNSUPPORTED, "sdpa_bwd_no_alloc: device %d beyond the %d supported", dev,
-                    kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return fail(SDPA_ERR_CUDA, "sdpa_bwd_no_alloc: cannot resolve the scratch array on device %d (%s)",
-                        dev, cudaGetErrorString(e));
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return SDPA_OK;
 }
 
@@ -645,6 +628,14 @@ sdpa_status_t sdpa_bwd_no_alloc(const sdpa_bwd_params* params, void* stream)
     return sdpa_bwd_gqa_reduce(p, ws, n, stream);
 }
 
+sdpa_status_t sdpa_bwd_no_alloc_check_status(void* stream)
+{
+    void* ws = nullptr;
+    const sdpa_status_t st = no_alloc_scratch(&ws);
+    if (st != SDPA_OK) return st;
+    return sdpa_bwd_check_status(ws, stream);
+}
+
 size_t sdpa_bwd_params_bytes(void) { return sizeof(sdpa_bwd_params); }
 
 int32_t sdpa_bwd_tile_kv(void) { return swa::kTileKV; }
@@ -675,33 +666,19 @@ namespace {
 
 // The forward's device status word (timeouts), one per device; as for the
 // allocation-free scratch above, host code takes its device address from
-// cudaGetSymbolAddress, once per device.
+// cudaGetSymbolAddress on every call. Every forward on a device shares it.
 static __device__ int32_t g_fwd_status;
-std::mutex g_fwd_mutex;
-int32_t* g_fwd_status_addr[kMaxDevices] = {};
 
 sdpa_status_t fwd_status_word(int32_t** out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fwd_status);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
-        return fail(SDPA_ERR_CUDA, "sdpa_fwd: no current CUDA device (%s)", cudaGetErrorString(e));
+        return fail(SDPA_ERR_CUDA, "sdpa_fwd: cannot resolve the status word on the current device (%s)",
+                    cudaGetErrorString(e));
     }
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(SDPA_ERR_UNSUPPORTED, "sdpa_fwd: device %d beyond the %d supported", dev, kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_fwd_mutex);
-    if (g_fwd_status_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fwd_status);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return fail(SDPA_ERR_CUDA, "sdpa_fwd: cannot resolve the status word on device %d (%s)", dev,
-                        cudaGetErrorString(e));
-        }
-        g_fwd_status_addr[dev] = static_cast<int32_t*>(p);
-    }
-    *out = g_fwd_status_addr[dev];
+    *out = static_cast<int32_t*>(p);
     return SDPA_OK;
 }
 

@@ -64,6 +64,14 @@ SMALL = [
          thd_lens=[390, 64, 1000], slot_align=8, det=True, seed=23),
     Case("br_nonsquare_q128_kv1100_w800_det_slots", 2, 8, 2, 128, 1100, 64, "br", 800, det=True,
          seed=25),
+    # strip mode (at most two visitors per q-tile) with THD tiles that end past
+    # their slot (row-wise dQ paths): GQA pairs through the accumulator rows, and
+    # 40 one-head sequences over more items than SMs (pairs inside a CTA's run
+    # adding in tensor memory, pairs split between CTAs)
+    Case("thd_strip_gqa4x2_w100_rowwise", 0, 4, 2, 0, 0, 64, "tl", 100, layout="thd",
+         thd_lens=[390, 64, 1000, 129], slot_align=8, seed=26),
+    Case("thd_strip_mha_40seq_w128_rowwise_det", 0, 1, 1, 0, 0, 64, "tl", 128, layout="thd",
+         thd_lens=[300 + (37 * i) % 300 for i in range(40)], slot_align=8, det=True, seed=27),
 ]
 
 
@@ -166,6 +174,14 @@ FULL = [
           gen_device="cuda"), [(2, 9)]),
     (Case("gqa_b24_h28x4_d128_s128_br_w8000_f16", 24, 28, 4, 128, 128, 128, "br", 8000,
           dtype="f16", seed=1006, gen_device="cuda"), [(bi, g) for bi in range(24) for g in range(4)]),
+    # the gpt_oss shape at the other lengths the pages sweep (S = 2k, 32k), and
+    # the b12 h48/6 d128 shape in f16
+    (Case("gptoss_b2_h16_d64_w128_s2048", 2, 16, 16, 2048, 2048, 64, "tl", 128, seed=1007,
+          gen_device="cuda"), [(0, 5), (1, 11)]),
+    (Case("gptoss_b2_h16_d64_w128_s32768", 2, 16, 16, 32768, 32768, 64, "tl", 128, seed=1008,
+          gen_device="cuda"), [(1, 7)]),
+    (Case("gqa_b12_h48x6_d128_s16484_br_w96_f16", 12, 48, 6, 16484, 16484, 128, "br", 96,
+          dtype="f16", seed=1009, gen_device="cuda"), [(3, 2)]),
 ]
 
 
@@ -190,3 +206,42 @@ def test_thd_varlen_sinks_det_full_size():
     bt = build(case, units=units)
     out = run_gpu(bt)
     check_all(bt, out)
+
+
+def _three_runs_bitwise(bt):
+    runs = [run_gpu(bt) for _ in range(3)]
+    for r in runs[1:]:
+        for name, a, b in zip(("dq", "dk", "dv", "dsink"), runs[0], r):
+            if a is not None:
+                assert torch.equal(a, b), f"{bt.case.name}: {name} differs between runs"
+    return runs[0]
+
+
+def test_full_size_deterministic_is_bitwise_repeatable():
+    """Deterministic mode at the gpt_oss headline size (b2 h16 d64 S8192 W128):
+    three backward passes give the same bits (cuDNN-frontend PR #866,
+    "Tests": bitwise repeatable across three passes), and a sampled unit
+    matches the oracle."""
+    case = Case("gptoss_b2_h16_d64_w128_s8192_det3", 2, 16, 16, 8192, 8192, 64, "tl", 128,
+                det=True, seed=1010, gen_device="cuda")
+    bt = build(case, units=[(0, 9)])
+    out = _three_runs_bitwise(bt)
+    check_all(bt, out)
+    del bt, out
+    torch.cuda.empty_cache()
+
+
+def test_thd_varlen_sinks_det_full_size_bitwise_repeatable():
+    """The packed variable-length workload (16 sequences of U[128, 8192] tokens,
+    h 64/8, f16, sinks, deterministic): three passes give the same bits,
+    dSink included."""
+    from sliding_window_attention_sdpa_gb300 import inputs
+    lens = inputs.thd_lengths(16, 128, 8192, seed=1005).tolist()
+    case = Case("thd16_h64x8_d64_f16_tl_w128_sink_det3", 0, 64, 8, 0, 0, 64, "tl", 128,
+                dtype="f16", layout="thd", thd_lens=lens, slot_align=128, sink=True, det=True,
+                seed=1011, gen_device="cuda")
+    bt = build(case, units=[(bi, 5) for bi in range(16)])
+    out = _three_runs_bitwise(bt)
+    check_all(bt, out)
+    del bt, out
+    torch.cuda.empty_cache()

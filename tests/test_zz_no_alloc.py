@@ -6,8 +6,11 @@ cudaMalloc's synchronisation, a deployment that forbids allocation after
 start-up): it runs the whole backward with a fixed scratch array inside the
 library instead of a caller-provided workspace. These tests check, through the
 C ABI, that two calls in a row give the same gradients as the workspace entry
-points (within the bf16 tolerance of the other parity tests), and that a
-problem too large for the fixed scratch is refused on the host.
+points (within the bf16 tolerance of the other parity tests) and as the fp64
+oracle, that deterministic mode still gives bitwise-repeatable gradients when
+its per-visitor slots do not fit the scratch, that the device status of a run
+can be read back without a workspace, and that a problem too large for the
+fixed scratch is refused on the host.
 
 This file is named to be collected last, so that a run stopping at the first
 failure has already run every other test.
@@ -19,7 +22,7 @@ import pytest
 import torch
 
 import sliding_window_attention_sdpa_gb300 as swa
-from swa_cases import Case, build, compare
+from swa_cases import Case, build, check_all, compare
 
 
 def test_oversized_problem_is_refused_on_the_host():
@@ -82,3 +85,70 @@ def test_no_alloc_matches_workspace_entry_points_twice():
         torch.cuda.synchronize()
         for name, got, w in zip(("dq", "dk", "dv", "dsink"), (dq, dk, dv, dsink), want):
             compare(f"call {call} {name}", got, w, case.dtype)
+        # and the oracle's gradients, element by element
+        check_all(bt, (dq, dk, dv, dsink))
+        assert swa.sdpa_bwd_no_alloc_check_status(stream) == swa.SDPA_OK, swa.last_error()
+
+
+def _no_alloc(d, kw, stream, **over):
+    """One sdpa_bwd_no_alloc call into fresh NaN-filled outputs."""
+    kw = dict(kw)
+    kw.update(over)
+    kw.pop("sink", None)
+    dq, dk, dv = (torch.full_like(d[n], float("nan")) for n in ("q", "k", "v"))
+    p = swa.make_params(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], dq, dk, dv, **kw)
+    rc = swa.sdpa_bwd_no_alloc(p, stream)
+    assert rc == swa.SDPA_OK, swa.last_error()
+    torch.cuda.synchronize()
+    return dq, dk, dv, p
+
+
+@pytest.mark.gpu
+def test_no_alloc_deterministic_without_slots_is_bitwise_repeatable():
+    """Deterministic mode 1 whose per-visitor dQ slots exceed the fixed scratch
+    runs as mode 2 (the relay): two calls give the same bits, the bits of the
+    workspace entry points in mode 2, and the oracle's gradients."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    swa.load()
+    case = Case("no_alloc_det_w1024", 1, 4, 4, 4096, 4096, 64, "tl", 1024, det=True, seed=32)
+    bt = build(case)
+    d = bt.dev
+    stream = torch.cuda.current_stream().cuda_stream
+    runs = []
+    for _ in range(2):
+        dq, dk, dv, p = _no_alloc(d, bt.kwargs, stream, deterministic=1)
+        runs.append((dq, dk, dv))
+    p.deterministic = 1
+    assert swa.sdpa_bwd_workspace_bytes(p) > swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+    p.deterministic = 2
+    assert swa.sdpa_bwd_workspace_bytes(p) <= swa.SDPA_BWD_NO_ALLOC_MAX_BYTES
+    ref = swa.backward(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], check_status=True,
+                       **dict(bt.kwargs, deterministic=2))
+    torch.cuda.synchronize()
+    for a, b, r in zip(runs[0], runs[1], ref[:3]):
+        assert torch.equal(a, b) and torch.equal(a, r)
+    check_all(bt, (*runs[0], None))
+    assert swa.sdpa_bwd_no_alloc_check_status(stream) == swa.SDPA_OK, swa.last_error()
+
+
+@pytest.mark.gpu
+def test_no_alloc_status_reports_lengths_longer_than_the_slot():
+    """A sequence length above s_q is clamped on the device (no access past the
+    slot) and reported through sdpa_bwd_no_alloc_check_status; the next valid
+    call reports SDPA_OK again."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    swa.load()
+    case = Case("no_alloc_bad_len", 2, 2, 2, 256, 256, 64, "tl", 64, lens_q=[256, 200],
+                lens_kv=[256, 200], seed=33)
+    bt = build(case)
+    d = bt.dev
+    stream = torch.cuda.current_stream().cuda_stream
+    bad = torch.tensor([256 + 5, 200], dtype=torch.int32, device=d["q"].device)
+    _no_alloc(d, bt.kwargs, stream, seq_q_lens=bad)
+    assert swa.sdpa_bwd_no_alloc_check_status(stream) == swa.SDPA_ERR_BAD_LENGTHS
+    assert "length" in swa.last_error()
+    dq, dk, dv, _ = _no_alloc(d, bt.kwargs, stream)
+    assert swa.sdpa_bwd_no_alloc_check_status(stream) == swa.SDPA_OK, swa.last_error()
+    check_all(bt, (dq, dk, dv, None))
