@@ -46,6 +46,7 @@ from sliding_window_attention_sdpa_gb300 import inputs  # noqa: E402
 
 WORKLOADS = {
     # name: (b, h_q, h_kv, s_q, s_kv, d, mask, window_left, dtype)
+    "tiny_b1_h2_d64_s256_tl_w32": (1, 2, 2, 256, 256, 64, "tl", 32, "bf16"),
     "gptoss_b2_h16_d64_w128_s2048": (2, 16, 16, 2048, 2048, 64, "tl", 128, "bf16"),
     "gptoss_b2_h16_d64_w128_s4096": (2, 16, 16, 4096, 4096, 64, "tl", 128, "bf16"),
     "gptoss_b2_h16_d64_w128_s8192": (2, 16, 16, 8192, 8192, 64, "tl", 128, "bf16"),
@@ -54,6 +55,13 @@ WORKLOADS = {
     "gqa_b24_h28x4_d128_s128_br_w8000": (24, 28, 4, 128, 128, 128, "br", 8000, "f16"),
     "nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000": (12, 40, 8, 128, 8960, 64, "br", 8000, "bf16"),
     "winonly_b4_h16_d64_s4096_w512": (4, 16, 16, 4096, 4096, 64, "none", 512, "bf16"),
+}
+# Packed variable-length (THD) workloads: n sequences with lengths drawn
+# uniformly from [lo, hi], each in a slot padded to a multiple of `align`
+# tokens (the gap tokens hold N(0, 1) values, never read into a result).
+THD_WORKLOADS = {
+    "thd16_h64x8_d64_f16_w128_sink_det": dict(n=16, lo=128, hi=8192, h_q=64, h_kv=8, d=64, mask="tl",
+                                             w=128, dtype="f16", sink=True, det=True, seed=1005, align=128),
 }
 DEFAULT = "gptoss_b2_h16_d64_w128_s8192"
 MODE = {"none": 0, "tl": 1, "br": 2}
@@ -85,14 +93,43 @@ def attended_pairs(s_q: int, s_kv: int, mask: str, w: int) -> int:
     return int(np.clip(hi - lo + 1, 0, None).sum())
 
 
-def algorithmic_bytes(b, h_q, h_kv, s_q, s_kv, d, gqa: bool):
+def algorithmic_bytes(rows_q, rows_kv, h_q, h_kv, d):
     """Main kernel, inputs read once and outputs written once: per q-row per
     q-head Q, dO (2*2d B), LSE, D (8 B) and the fp32 dQ accumulation (4d B);
-    per kv-row per kv-head K, V (2*2d B) and dK, dV (2*2d B; fp32 partials
-    per q-head under GQA)."""
-    q_side = b * s_q * h_q * (2 * 2 * d + 8 + 4 * d)
-    kv_side = b * s_kv * h_kv * (2 * 2 * d) + (b * s_kv * h_q * 2 * 4 * d if gqa else b * s_kv * h_kv * 2 * 2 * d)
-    return q_side + kv_side
+    per kv-row per kv-head K, V (2*2d B) and dK, dV (2*2d B; the GQA group sum
+    is formed in tensor memory, so dK, dV are written once per kv-head)."""
+    return rows_q * h_q * (2 * 2 * d + 8 + 4 * d) + rows_kv * h_kv * 4 * 2 * d
+
+
+def spec(name: str) -> dict:
+    """Shape of a workload: BSHD (b, s_q, s_kv) or THD (sequence lengths and
+    slot offsets), heads, head dim, mask, window, dtype, sink, deterministic."""
+    if name in THD_WORKLOADS:
+        w = dict(THD_WORKLOADS[name])
+        lens = inputs.thd_lengths(w["n"], w["lo"], w["hi"], seed=w["seed"])
+        offs = inputs.thd_offsets(lens, w["align"])
+        slot = int(np.diff(offs).max())
+        w.update(layout="thd", b=w["n"], lens=lens, offs=offs, total=int(offs[-1]), s_q=slot, s_kv=slot)
+        return w
+    b, hq, hkv, sq, skv, d, mask, wl, dt = WORKLOADS[name]
+    return dict(layout="bshd", b=b, h_q=hq, h_kv=hkv, s_q=sq, s_kv=skv, d=d, mask=mask, w=wl, dtype=dt,
+                sink=False, det=False, lens=None, offs=None, total=None, seed=1002)
+
+
+def workload_flops(sp: dict) -> int:
+    """10 d FLOPs per attended (q, k) pair and q-head."""
+    if sp["layout"] == "thd":
+        pairs = sum(attended_pairs(int(L), int(L), sp["mask"], sp["w"]) for L in sp["lens"])
+        return 10 * sp["d"] * pairs * sp["h_q"]
+    return 10 * sp["d"] * attended_pairs(sp["s_q"], sp["s_kv"], sp["mask"], sp["w"]) * sp["b"] * sp["h_q"]
+
+
+def workload_rows(sp: dict):
+    """Token rows that carry data: (q rows, kv rows)."""
+    if sp["layout"] == "thd":
+        n = int(np.sum(sp["lens"]))
+        return n, n
+    return sp["b"] * sp["s_q"], sp["b"] * sp["s_kv"]
 
 
 class Problem:
@@ -101,36 +138,54 @@ class Problem:
     def __init__(self, name: str, device, seed: int, deterministic: bool = False):
         import sliding_window_attention_sdpa_gb300 as swa
         self.swa = swa
-        b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
+        sp = self.sp = spec(name)
+        b, hq, hkv, sq, skv, d = sp["b"], sp["h_q"], sp["h_kv"], sp["s_q"], sp["s_kv"], sp["d"]
+        mask, w, dt = sp["mask"], sp["w"], sp["dtype"]
         self.name, self.b, self.h_q, self.h_kv, self.s_q, self.s_kv, self.d = name, b, hq, hkv, sq, skv, d
         self.mask, self.w, self.dtype = mask, w, dt
+        self.deterministic = bool(deterministic or sp["det"])
         self.scale = 1.0 / math.sqrt(d)
-        t = inputs.make_tensors((b, sq, hq, d), (b, skv, hkv, d), hq, dt, seed, False, device=device)
-        self.q, self.k, self.v, self.do = t.q, t.k, t.v, t.do
+        thd = sp["layout"] == "thd"
+        if thd:
+            seed = sp["seed"]
+            qs, kvs = (sp["total"], hq, d), (sp["total"], hkv, d)
+            lse_shape = (hq, sp["total"])
+        else:
+            qs, kvs = (b, sq, hq, d), (b, skv, hkv, d)
+            lse_shape = (b, hq, sq)
+        t = inputs.make_tensors(qs, kvs, hq, dt, seed, sp["sink"], device=device)
+        self.q, self.k, self.v, self.do, self.sink = t.q, t.k, t.v, t.do, t.sink
         # O and LSE with the magnitudes of a real forward over ~(w+1) keys of
         # N(0,1) logits: O ~ N(0, 1/n), LSE = log(n) + 1/2.
         n = (w + 1) if w >= 0 else skv
         n = min(n, skv)
-        self.o = (inputs.randn((b, sq, hq, d), seed * 16 + 6, torch.float32, device)
-                  / math.sqrt(n)).to(inputs.DTYPES[dt])
-        self.lse = torch.full((b, hq, sq), math.log(n) + 0.5, dtype=torch.float32, device=device)
+        self.o = (inputs.randn(qs, seed * 16 + 6, torch.float32, device) / math.sqrt(n)).to(inputs.DTYPES[dt])
+        self.lse = torch.full(lse_shape, math.log(n) + 0.5, dtype=torch.float32, device=device)
         self.dq = torch.empty_like(self.q)
         self.dk = torch.empty_like(self.k)
         self.dv = torch.empty_like(self.v)
+        self.dsink = torch.empty(hq, dtype=torch.float32, device=device) if sp["sink"] else None
+        # keyword arguments of the binding's backward()/make_params() besides the tensors
+        self.kw = dict(scale=self.scale, mask_mode=MODE[mask], window_left=w)
+        if thd:
+            offs = torch.from_numpy(sp["offs"].astype(np.int32)).to(device)
+            lens = torch.from_numpy(sp["lens"].astype(np.int32)).to(device)
+            self.kw.update(q_offsets=offs, kv_offsets=offs, seq_q_lens=lens, seq_kv_lens=lens,
+                           max_seqlen_q=sq, max_seqlen_kv=skv)
         self.params = swa.make_params(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
-                                      self.dk, self.dv, scale=self.scale, mask_mode=MODE[mask],
-                                      window_left=w, deterministic=deterministic)
+                                      self.dk, self.dv, deterministic=self.deterministic,
+                                      sink=self.sink, dsink=self.dsink, **self.kw)
         self.ws = swa.alloc_workspace(self.params, device)
         # the forward on the same inputs (its own outputs)
         self.fo = torch.empty_like(self.q)
         self.flse = torch.empty_like(self.lse)
-        self.fparams = swa.make_fwd_params(self.q, self.k, self.v, self.fo, self.flse, scale=self.scale,
-                                           mask_mode=MODE[mask], window_left=w)
-        self.fwd_flops = 4 * d * attended_pairs(sq, skv, mask, w) * b * hq
+        self.fparams = swa.make_fwd_params(self.q, self.k, self.v, self.fo, self.flse, sink=self.sink, **self.kw)
+        rows_q, rows_kv = workload_rows(sp)
+        self.flops = workload_flops(sp)
+        self.fwd_flops = self.flops * 4 // 10
         # Q, K, V read once, O and LSE written once
-        self.fwd_bytes = b * sq * hq * (2 * 2 * d + 4) + b * skv * hkv * 2 * 2 * d
-        self.flops = 10 * d * attended_pairs(sq, skv, mask, w) * b * hq
-        self.main_bytes = algorithmic_bytes(b, hq, hkv, sq, skv, d, hq != hkv)
+        self.fwd_bytes = rows_q * hq * (2 * 2 * d + 4) + rows_kv * hkv * 2 * 2 * d
+        self.main_bytes = algorithmic_bytes(rows_q, rows_kv, hq, hkv, d)
 
     def step(self, stream: int, ev=None):
         """The whole backward; `ev` = (before_main, after_main) events."""
@@ -309,14 +364,14 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
     direction on its own (GB/s), which bound the pipelined step from below.
     """
     import sliding_window_attention_sdpa_gb300 as swa
-    names = (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse)
+    names = (prob.q, prob.k, prob.v, prob.o, prob.do, prob.lse) + ((prob.sink,) if prob.sink is not None else ())
+    outs = (prob.dq, prob.dk, prob.dv) + ((prob.dsink,) if prob.dsink is not None else ())
     host_in = [t.cpu().pin_memory() for t in names]
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (prob.dq, prob.dk, prob.dv)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     dev_in = [[torch.empty_like(t) for t in names] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    kw = dict(scale=prob.scale, mask_mode=MODE[prob.mask], window_left=prob.w,
-              workspace=prob.ws)
+    kw = dict(prob.kw, workspace=prob.ws, deterministic=prob.deterministic)
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
@@ -332,11 +387,13 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
         copied[buf].record(s_in)
         s_run.wait_event(copied[buf])
         with torch.cuda.stream(s_run):
-            dq, dk, dv, _ = swa.backward(*dev_in[buf], **kw)
+            ins = dev_in[buf]
+            res = swa.backward(*ins[:6], sink=ins[6] if len(ins) > 6 else None, **kw)
+            res = tuple(x for x in res if x is not None)
         done[buf].record(s_run)
         s_out.wait_event(done[buf])
         with torch.cuda.stream(s_out):
-            for h, d in zip(host_out, (dq, dk, dv)):
+            for h, d in zip(host_out, res):
                 d.record_stream(s_out)
                 h.copy_(d, non_blocking=True)
 
@@ -365,43 +422,75 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
         return nbytes / (sorted(out)[reps // 2] * 1e-3) / 1e9
 
     link = {"h2d_gbs": alone(s_in, list(zip(dev_in[0], host_in)), h2d),
-            "d2h_gbs": alone(s_out, list(zip(host_out, (prob.dq, prob.dk, prob.dv))), d2h)}
+            "d2h_gbs": alone(s_out, list(zip(host_out, outs)), d2h)}
     return ms, h2d, d2h, link
 
 
 def cpu_oracle_step(name: str, nthreads: int, units=None):
     """One fp64 oracle backward (window-bounded sweep) of the workload on the
-    host cores; returns (seconds, fraction of the workload's units run)."""
+    host cores; returns (seconds, fraction of the workload's FLOPs run).
+    `units` limits the run to the first (sequence, kv-head) units."""
     import oracle
-    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
-    t = inputs.make_tensors((b, sq, hq, d), (b, skv, hkv, d), hq, dt, 7, False)
+    sp = spec(name)
+    b, hq, hkv, d = sp["b"], sp["h_q"], sp["h_kv"], sp["d"]
     f64 = lambda x: x.double().numpy()
-    n = min((w + 1) if w >= 0 else skv, skv)
-    o = (inputs.randn((b, sq, hq, d), 7 * 16 + 6) / math.sqrt(n)).to(inputs.DTYPES[dt])
-    lse = np.full((b, hq, sq), math.log(n) + 0.5)
-    p = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s_q=sq, s_kv=skv, d=d, scale=1 / math.sqrt(d),
-                       mask_mode=MODE[mask], window_left=w, nthreads=nthreads)
+    n = min((sp["w"] + 1) if sp["w"] >= 0 else sp["s_kv"], sp["s_kv"])
+    kw = dict(b=b, h_q=hq, h_kv=hkv, s_q=sp["s_q"], s_kv=sp["s_kv"], d=d, scale=1 / math.sqrt(d),
+              mask_mode=MODE[sp["mask"]], window_left=sp["w"], nthreads=nthreads, has_sink=sp["sink"])
+    if sp["layout"] == "thd":
+        qs, kvs, lse_shape = (sp["total"], hq, d), (sp["total"], hkv, d), (hq, sp["total"])
+        kw.update(layout=oracle.THD, seq_q_lens=sp["lens"], seq_kv_lens=sp["lens"],
+                  q_offsets=sp["offs"], kv_offsets=sp["offs"])
+    else:
+        qs, kvs, lse_shape = (b, sp["s_q"], hq, d), (b, sp["s_kv"], hkv, d), (b, hq, sp["s_q"])
+    t = inputs.make_tensors(qs, kvs, hq, sp["dtype"], 7, sp["sink"])
+    o = (inputs.randn(qs, 7 * 16 + 6) / math.sqrt(n)).to(inputs.DTYPES[sp["dtype"]])
+    lse = np.full(lse_shape, math.log(n) + 0.5)
+    p = oracle.Problem(**kw)
     frac = 1.0
     if units is not None and units < b * hkv:
         m = np.zeros(b * hkv, np.uint8)
         m[:units] = 1
         p.unit_mask = m
-        frac = units / (b * hkv)
+        if sp["layout"] == "thd":
+            # units are (sequence, kv-head), sequence-major: FLOPs of the sampled ones
+            pairs = [attended_pairs(int(L), int(L), sp["mask"], sp["w"]) for L in sp["lens"]]
+            done = sum(pairs[u // hkv] for u in range(units))
+            frac = done / (sum(pairs) * hkv)
+        else:
+            frac = units / (b * hkv)
     args = (f64(t.q), f64(t.k), f64(t.v), f64(o), f64(t.do), lse)
+    sink = f64(t.sink) if t.sink is not None else None
     t0 = time.perf_counter()
-    oracle.backward(p, *args)
+    oracle.backward(p, *args, sink)
     return time.perf_counter() - t0, frac
 
 
 def cpu_units_for_budget(name: str, budget_s: float, nthreads: int):
-    """Units (batch, kv-head) that fit about `budget_s` seconds of oracle time."""
-    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
-    total = b * hkv
+    """Units (sequence, kv-head) that fit about `budget_s` seconds of oracle time."""
+    sp = spec(name)
+    total = sp["b"] * sp["h_kv"]
     probe = max(1, min(total, nthreads))
     t, frac = cpu_oracle_step(name, nthreads, probe)
     per_unit_wave = t  # one wave of `probe` units in parallel
     waves = max(1, int(budget_s / max(per_unit_wave, 1e-3)))
     return min(total, probe * waves)
+
+
+# Single-thread oracle figures the CPU baseline reports beside the all-core
+# one: the tiny case whole, and the gpt_oss shape at S = 2048 on one
+# (batch, head) unit of its 32.
+SINGLE_THREAD = {"tiny_b1_h2_d64_s256_tl_w32": None, "gptoss_b2_h16_d64_w128_s2048": 1}
+
+
+def single_thread_figures():
+    out = {}
+    for name, units in SINGLE_THREAD.items():
+        sec, frac = cpu_oracle_step(name, 1, units)
+        flops = workload_flops(spec(name)) * frac
+        out[name] = {"value": flops / sec / 1e9, "unit": "GFLOP/s", "cores": 1,
+                     "sample": "whole workload" if units is None else f"{units} (batch, kv-head) unit"}
+    return out
 
 
 def reference_arm(args, rank, world):
@@ -419,8 +508,9 @@ def reference_arm(args, rank, world):
     for _ in range(args.steps):
         t, frac = cpu_oracle_step(name, cores, units)
         times.append(t)
-    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
-    flops = 10 * d * attended_pairs(sq, skv, mask, w) * b * hq * frac
+    sp = spec(name)
+    flops = workload_flops(sp) * frac
+    b, hkv = sp["b"], sp["h_kv"]
     sec = statistics.mean(times)
     val = flops / sec / 1e12
     line = {
@@ -441,13 +531,19 @@ METRIC = "SWA bwd attended TFLOP/s (b2 h16 d64 W128 S8k bf16)"
 
 
 def workload_config(name):
-    b, hq, hkv, sq, skv, d, mask, w, dt = WORKLOADS[name]
-    return {"workload": name, "global_batch": b, "seq_len": sq, "seq_len_kv": skv, "heads_q": hq,
-            "heads_kv": hkv, "head_dim": d, "mask": {"tl": "top_left_causal",
-                                                     "br": "bottom_right_causal",
-                                                     "none": "window_only"}[mask],
-            "window_left": w, "l2": "flushed between timed steps (512 MB write, then 512 MB read of another buffer)",
-            "parallelism": "replicas"}
+    sp = spec(name)
+    c = {"workload": name, "global_batch": sp["b"], "seq_len": sp["s_q"], "seq_len_kv": sp["s_kv"],
+         "heads_q": sp["h_q"], "heads_kv": sp["h_kv"], "head_dim": sp["d"],
+         "mask": {"tl": "top_left_causal", "br": "bottom_right_causal", "none": "window_only"}[sp["mask"]],
+         "window_left": sp["w"], "dtype": sp["dtype"],
+         "l2": "flushed between timed steps (512 MB write, then 512 MB read of another buffer)",
+         "parallelism": "replicas"}
+    if sp["layout"] == "thd":
+        c.update(layout="thd", sequences=sp["b"], tokens=int(np.sum(sp["lens"])), slot_tokens=sp["total"],
+                 lengths=f"uniform [{THD_WORKLOADS[name]['lo']}, {THD_WORKLOADS[name]['hi']}] (seed "
+                         f"{THD_WORKLOADS[name]['seed']}), slots padded to {THD_WORKLOADS[name]['align']}",
+                 sinks=sp["sink"])
+    return c
 
 
 def aggregate(per_rank_ms, per_rank_flops):
@@ -472,7 +568,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(THD_WORKLOADS))
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-log-dir", default=None,
@@ -533,7 +629,7 @@ def main():
         "main_kernel_ms": main_avg,
         "main_kernel_tflops": prob.flops / (main_avg * 1e-3) / 1e12,
         "tensor_peak_frac": prob.flops / (main_avg * 1e-3) / 1e12 / peak_tf,
-        "deterministic": bool(args.deterministic),
+        "deterministic": prob.deterministic,
         "device_status": int(status),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
                      "frac": achieved / peak_gbs, "traffic": measured_traffic(args.workload),
@@ -562,11 +658,12 @@ def main():
         units = cpu_units_for_budget(name, 15.0, cores)
         sec, frac = cpu_oracle_step(name, cores, units)
         cpu_val = prob.flops * frac / sec / 1e12
-        b, hq, hkv = WORKLOADS[name][:3]
+        sp = spec(name)
         line["cpu_baseline"] = {"value": cpu_val, "unit": "TFLOP/s", "cores": cores,
                                 "kind": "oracle",
-                                "sample": f"{units} of {b * hkv} (batch, kv-head) units, "
-                                          "fp64 window-bounded backward"}
+                                "sample": f"{units} of {sp['b'] * sp['h_kv']} (sequence, kv-head) units, "
+                                          "fp64 window-bounded backward",
+                                "single_thread": single_thread_figures()}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

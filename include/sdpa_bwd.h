@@ -54,7 +54,10 @@ typedef enum {
     SDPA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     SDPA_ERR_TIMEOUT = 4,      /* a deterministic-relay wait ran out on the device */
     SDPA_ERR_BAD_LENGTHS = 5,  /* device-side: a sequence length exceeds its slot */
-    SDPA_ERR_WORKSPACE = 6     /* workspace NULL, misaligned or too small */
+    SDPA_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or too small */
+    SDPA_ERR_BOUNDS = 7        /* device-side, range-checked build only (compiled with
+                                  -DSDPA_DEBUG_BOUNDS): a computed index fell outside its
+                                  buffer; the access was skipped */
 } sdpa_status_t;
 
 enum { SDPA_BF16 = 0, SDPA_F16 = 1 };
@@ -187,7 +190,9 @@ sdpa_status_t sdpa_bwd_gqa_reduce(const sdpa_bwd_params *params, void *workspace
  * backward run on `workspace`: SDPA_OK, SDPA_ERR_TIMEOUT (a device wait gave
  * up -- a dQ relay turn, the partial of a dQ pair split between two CTAs, or a
  * hand-off inside the main kernel, named by sdpa_bwd_last_error(); the
- * gradients are then incomplete), SDPA_ERR_BAD_LENGTHS, or SDPA_ERR_UNSUPPORTED (the
+ * gradients are then incomplete), SDPA_ERR_BAD_LENGTHS, SDPA_ERR_BOUNDS (a
+ * range-checked build found an index outside its buffer), or
+ * SDPA_ERR_UNSUPPORTED (the
  * device placed the main kernel's dynamic shared memory off a 1024-byte
  * boundary, which its swizzled tiles need; it then computed nothing).
  */

@@ -20,7 +20,7 @@ from typing import Optional
 from . import _build
 
 SDPA_OK, SDPA_ERR_INVALID_ARG, SDPA_ERR_UNSUPPORTED, SDPA_ERR_CUDA = 0, 1, 2, 3
-SDPA_ERR_TIMEOUT, SDPA_ERR_BAD_LENGTHS, SDPA_ERR_WORKSPACE = 4, 5, 6
+SDPA_ERR_TIMEOUT, SDPA_ERR_BAD_LENGTHS, SDPA_ERR_WORKSPACE, SDPA_ERR_BOUNDS = 4, 5, 6, 7
 SDPA_BF16, SDPA_F16 = 0, 1
 SDPA_BSHD, SDPA_THD = 0, 1
 SDPA_MASK_NONE, SDPA_MASK_TOP_LEFT, SDPA_MASK_BOTTOM_RIGHT = 0, 1, 2
@@ -82,7 +82,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The in-tree library, or the one SWA_SDPA_LIB names (e.g. the
+    range-checked build, libswa_sdpa_bwd_dbg.so)."""
+    return os.environ.get("SWA_SDPA_LIB") or _build.LIB
 
 
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -91,7 +93,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
+        path = library_path()
         if not os.path.exists(path):
             if not build_if_missing:
                 raise RuntimeError(

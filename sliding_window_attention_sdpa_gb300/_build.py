@@ -1,7 +1,10 @@
 """Builds the CUDA library libswa_sdpa_bwd.so in-tree with nvcc (sm_103a only).
 
 Each translation unit is compiled in parallel, then linked into one shared
-library that exports the C ABI of include/sdpa_bwd.h.
+library that exports the C ABI of include/sdpa_bwd.h. build(debug_bounds=True)
+builds the range-checked variant libswa_sdpa_bwd_dbg.so (-DSDPA_DEBUG_BOUNDS:
+every raw global index is checked against its buffer and an out-of-range one
+is reported as SDPA_ERR_BOUNDS instead of being accessed).
 """
 from __future__ import annotations
 
@@ -15,6 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswa_sdpa_bwd.so")
+LIB_DBG = os.path.join(BUILD, "libswa_sdpa_bwd_dbg.so")
+DEBUG_BOUNDS = ("-DSDPA_DEBUG_BOUNDS",)
 SOURCES = ["api.cu", "aux_kernels.cu", "main_kernel.cu", "fwd_kernel.cu"]
 HEADERS = ["ptx.cuh", "seq.cuh", "sdpa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -42,19 +47,23 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra=(), debug_bounds: bool = False) -> str:
     """Compile and link the library if any source changed; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "stamp")
+    if debug_bounds:
+        extra = tuple(extra) + DEBUG_BOUNDS
+    lib_path = LIB_DBG if debug_bounds else LIB
+    objdir = os.path.join(BUILD, "dbg") if debug_bounds else BUILD
+    os.makedirs(objdir, exist_ok=True)
+    stamp = os.path.join(objdir, "stamp")
     digest = _digest(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib_path
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         cmd = [nvcc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -68,17 +77,17 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

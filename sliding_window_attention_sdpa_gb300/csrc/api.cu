@@ -213,6 +213,41 @@ swa::Geometry geometry_of(const sdpa_bwd_params* p)
     return g;
 }
 
+// Elements reachable from a strided [b][s][h][d] (BSHD) or [t][h][d] (THD)
+// tensor's base pointer.
+int64_t tensor_extent(bool thd, const int64_t* st, int64_t b, int64_t s, int64_t h, int64_t d, int64_t total)
+{
+    if (thd) return total > 0 && h > 0 ? (total - 1) * st[1] + (h - 1) * st[2] + d : 0;
+    return b > 0 && s > 0 && h > 0 ? (b - 1) * st[0] + (s - 1) * st[1] + (h - 1) * st[2] + d : 0;
+}
+
+// Buffer extents for the range-checked build (the workspace sections from
+// `w`; null for the forward, which has none).
+swa::Extents extents_of(const sdpa_bwd_params* p, const swa::WsLayout* w)
+{
+    const bool thd = p->layout == SDPA_THD;
+    const int64_t nqt = (p->s_q + swa::kTileQ - 1) / swa::kTileQ;
+    swa::Extents e{};
+    e.q = tensor_extent(thd, p->q_stride, p->b, p->s_q, p->h_q, p->d, p->total_q);
+    e.o = tensor_extent(thd, p->o_stride, p->b, p->s_q, p->h_q, p->d, p->total_q);
+    e.dout = tensor_extent(thd, p->do_stride, p->b, p->s_q, p->h_q, p->d, p->total_q);
+    e.dq = tensor_extent(thd, p->dq_stride, p->b, p->s_q, p->h_q, p->d, p->total_q);
+    e.k = tensor_extent(thd, p->k_stride, p->b, p->s_kv, p->h_kv, p->d, p->total_kv);
+    e.v = tensor_extent(thd, p->v_stride, p->b, p->s_kv, p->h_kv, p->d, p->total_kv);
+    e.dk = tensor_extent(thd, p->dk_stride, p->b, p->s_kv, p->h_kv, p->d, p->total_kv);
+    e.dv = tensor_extent(thd, p->dv_stride, p->b, p->s_kv, p->h_kv, p->d, p->total_kv);
+    e.lse = thd ? p->h_q * p->total_q : p->b * p->h_q * p->s_q;
+    e.sink = p->sink ? p->h_q : 0;
+    if (w != nullptr) {
+        e.stats = p->b * p->h_q * nqt * swa::kTileQ * 2;
+        e.dq_acc = rows_q(p) * p->h_q * p->d;
+        e.dq_part = p->b * p->h_q * nqt * w->n_slots * swa::kTileQ * p->d;
+        e.dsink_part = p->sink ? p->h_q * w->n_row_blocks : 0;
+        e.sems = w->n_sems;
+    }
+    return e;
+}
+
 // Full check before a launch: shapes, strides, pointers and workspace.
 sdpa_status_t check_all(const sdpa_bwd_params* p, const void* ws, size_t ws_bytes)
 {
@@ -389,6 +424,7 @@ sdpa_status_t sdpa_bwd_preprocess(const sdpa_bwd_params* p, void* ws, size_t ws_
     const swa::WsLayout w = layout_of(p);
     swa::PreArgs a{};
     a.g = geometry_of(p);
+    a.g.ext = extents_of(p, &w);
     a.o = p->o;
     a.dout = p->dout;
     a.lse = p->lse;
@@ -432,6 +468,7 @@ sdpa_status_t sdpa_bwd(const sdpa_bwd_params* p, void* ws, size_t ws_bytes, void
     const swa::WsLayout w = layout_of(p);
     swa::MainArgs a{};
     a.g = geometry_of(p);
+    a.g.ext = extents_of(p, &w);
     a.q = p->q;
     a.k = p->k;
     a.v = p->v;
@@ -513,6 +550,8 @@ sdpa_status_t sdpa_bwd_dq_convert(const sdpa_bwd_params* p, void* ws, size_t ws_
     const swa::WsLayout w = layout_of(p);
     swa::CvtArgs a{};
     a.g = geometry_of(p);
+    a.g.ext = extents_of(p, &w);
+    a.status = at<int32_t>(ws, w.status);
     a.dq_acc = at<float>(ws, w.dq_acc);
     a.dq_part = at<float>(ws, w.dq_part);
     a.n_slots = w.n_slots;
@@ -554,6 +593,8 @@ sdpa_status_t sdpa_bwd_check_status(const void* ws, void* stream)
                                                  : "a hand-off inside the main kernel");
     if (host[0] == SDPA_ERR_BAD_LENGTHS)
         return fail(SDPA_ERR_BAD_LENGTHS, "a sequence length exceeds its slot (or s_q/s_kv)");
+    if (host[0] == SDPA_ERR_BOUNDS)
+        return fail(SDPA_ERR_BOUNDS, "a device index fell outside its buffer (range-checked build); the access was skipped");
     if (host[0] == SDPA_ERR_UNSUPPORTED)
         return fail(SDPA_ERR_UNSUPPORTED, "the device gave the main kernel shared memory not 1024-byte aligned");
     if (host[0] != 0) return fail(SDPA_ERR_CUDA, "unknown device status %d", host[0]);
@@ -755,6 +796,7 @@ sdpa_status_t sdpa_fwd(const sdpa_fwd_params* f, void* stream)
     swa::FwdArgs a{};
     if ((st = fwd_status_word(&a.status)) != SDPA_OK) return st;
     a.g = geometry_of(&p);
+    a.g.ext = extents_of(&p, nullptr);
     a.o = f->o;
     a.lse = f->lse;
     a.sink = f->sink;
@@ -793,6 +835,8 @@ sdpa_status_t sdpa_fwd_check_status(void* stream)
     if (host == 0) return SDPA_OK;
     if ((st = cuda_status(cudaMemset(word, 0, sizeof(int32_t)), "status reset")) != SDPA_OK) return st;
     if (host == SDPA_ERR_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a forward wait ran out on the device");
+    if (host == SDPA_ERR_BOUNDS)
+        return fail(SDPA_ERR_BOUNDS, "a forward index fell outside its buffer (range-checked build)");
     if (host == SDPA_ERR_UNSUPPORTED)
         return fail(SDPA_ERR_UNSUPPORTED, "the device gave the forward kernel shared memory not 1024-byte aligned");
     return fail(SDPA_ERR_CUDA, "unknown forward device status %d", host);

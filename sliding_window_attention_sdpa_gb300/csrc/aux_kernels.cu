@@ -167,7 +167,10 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
         // the row's LSE, loaded before the wait for the box
         float lse = -INFINITY;
         if (valid && half == 0)
-            lse = __ldg(a.lse + (thd ? h * g.rows_q + s.q_row0 + i : (b.bi * g.h_q + h) * g.s_q + i));
+        {
+            const float* pl = a.lse + (thd ? h * g.rows_q + s.q_row0 + i : (b.bi * g.h_q + h) * g.s_q + i);
+            if (in_bounds(a.status, pl, a.lse, g.ext.lse, 1)) lse = __ldg(pl);
+        }
         // q-tiles with three or more visitors take unordered atomics (unless
         // deterministic): their accumulator rows start at zero
         bool zero_acc = false;
@@ -199,9 +202,12 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
         }
         if constexpr (TPU == 2) part += __shfl_xor_sync(0xffffffffu, part, 1);
         if (zero_acc && valid) {
-            float4* z = reinterpret_cast<float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + half * 64);
+            float* zf = a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + half * 64;
+            float4* z = reinterpret_cast<float4*>(zf);
+            if (in_bounds(a.status, zf, a.dq_acc, g.ext.dq_acc, 64)) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 16; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         if (unit && half == 0) {
             // per-row statistics for the main kernel, one slot for every row of
@@ -211,11 +217,14 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
             float nl2 = -INFINITY, ds = 0.f;
             if (valid && lse != -INFINITY) {
                 nl2 = -(lse * 1.4426950408889634f);
-                if (with_sink) ds = -expf(a.sink[h] - lse) * part;
+                if (with_sink && in_bounds(a.status, a.sink + h, a.sink, g.ext.sink, 1))
+                    ds = -expf(a.sink[h] - lse) * part;
             }
             float* srow = a.stats + 2 * ((b.bi * g.h_q + h) * a.stats_row + (i & ~int64_t(kTileQ - 1))) + (i & (kTileQ - 1));
-            srow[0] = nl2;
-            srow[kTileQ] = valid ? -part : 0.f;
+            if (in_bounds(a.status, srow, a.stats, g.ext.stats, kTileQ + 1)) {
+                srow[0] = nl2;
+                srow[kTileQ] = valid ? -part : 0.f;
+            }
             if (with_sink) red[(j & 1) * 256 + hl * rows_n + r] = ds;
         }
         __syncthreads();   // ring entry st is read; dSink terms are written
@@ -227,7 +236,8 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
             // this block's dSink partial of a head: its rows summed in order
             float t = 0.f;
             for (int k = 0; k < rows_n; ++k) t += red[(j & 1) * 256 + tid * rows_n + k];
-            a.dsink_part[(b.hc * hc_n + tid) * a.n_row_blocks + static_cast<int64_t>(b.bi) * nrb + b.rb] = t;
+            float* pd = a.dsink_part + (b.hc * hc_n + tid) * a.n_row_blocks + static_cast<int64_t>(b.bi) * nrb + b.rb;
+            if (in_bounds(a.status, pd, a.dsink_part, g.ext.dsink_part, 1)) *pd = t;
         }
         if (++st == n_stages) {
             st = 0;
@@ -239,85 +249,112 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
 // ---------------------------------------------------------------- convert
 // The main kernel already stored dQ for every q-tile some kv-tile visits (its
 // last visitor converts). This writes dQ = 0 on the other rows of a slot:
-// rows past the sequence's length and q-tiles no kv-tile visits. grid
-// (ceil(s_q / 128), h_q, b). It also finishes dSink in a fixed order.
+// rows past the sequence's length and q-tiles no kv-tile visits; converts the
+// q-tiles whose visitors added with unordered atomics, and sums (in visitor
+// order) and converts those whose visitors stored per-visitor partials. It
+// also finishes dSink in a fixed order. Persistent: CTA c walks the
+// (q-head, q-tile, sequence) tiles c, c + grid, ..., head fastest (one
+// [row][head][d] row holds every head), so that a grid of a few waves covers
+// problems whose tiles mostly need nothing.
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
 {
-    constexpr int TPR = HD / 8;
-    constexpr int RPP = 256 / TPR;
+    constexpr int TPR = HD / 8;         // threads per row (8 values each)
+    constexpr int RPP = 256 / TPR;      // rows per pass
+    constexpr int PASSES = kTileQ / RPP;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
     const int c = tid % TPR;
-    const int64_t j = blockIdx.x, h = blockIdx.y, bi = blockIdx.z;
-    if (a.dsink != nullptr && j == 0 && h == 0 && bi == 0) {
+    if (a.dsink != nullptr && blockIdx.x == 0) {
         // fixed-order finish, a warp per head: lane l sums partials l, l + 32,
         // ... in order, then a fixed butterfly; bitwise repeatable
         const int lane = tid & 31;
         for (int64_t hh = tid >> 5; hh < g.h_q; hh += blockDim.x >> 5) {
             float t = 0.f;
-            for (int64_t k = lane; k < a.n_row_blocks; k += 32) t += a.dsink_part[hh * a.n_row_blocks + k];
+            for (int64_t k = lane; k < a.n_row_blocks; k += 32)
+                if (in_bounds(a.status, a.dsink_part + hh * a.n_row_blocks + k, a.dsink_part, g.ext.dsink_part, 1))
+                    t += a.dsink_part[hh * a.n_row_blocks + k];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
             if (lane == 0) a.dsink[hh] = t;
         }
     }
-    const SeqInfo s = seq_info(g, bi);
-    const int64_t t0 = j * kTileQ;
-    const int64_t t1 = imin(t0 + kTileQ, s.slot_q);
-    if (t0 >= t1) return;
-    int64_t z0 = t0;  // first row to zero
-    bool accumulated = false, from_slots = false;
-    int64_t n_vis = 0;
-    if (t0 < s.len_q) {
-        int64_t first;
-        q_tile_visitors(g, s, j, first, n_vis);
-        if (n_vis > 0) z0 = s.len_q;
-        accumulated = n_vis >= 3 && !a.deterministic;
-        from_slots = n_vis >= 3 && a.deterministic && a.n_slots > 0;
-    }
     const bool thd = g.layout == 1;
     uint16_t* dq = static_cast<uint16_t*>(a.dq);
-    if (accumulated) {
-        // rows whose dQ was summed with unordered atomics: convert them
-        const int64_t e1 = imin(t1, s.len_q);
-#pragma unroll 1
-        for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
-            const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8);
-            const float4 x = src[0], y = src[1];
-            const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-            uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
-                            h * a.dq_stride[2] + c * 8;
-            *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
+    const uint32_t hq = static_cast<uint32_t>(g.h_q), nx = static_cast<uint32_t>(a.n_q_tiles);
+    const uint32_t n_tiles = hq * nx * static_cast<uint32_t>(g.b);
+    for (uint32_t u = blockIdx.x; u < n_tiles; u += gridDim.x) {
+        const uint32_t rest = u / hq, bq = rest / nx;
+        const int64_t h = u - rest * hq, j = rest - bq * nx, bi = bq;
+        const SeqInfo s = seq_info(g, bi);
+        const int64_t t0 = j * kTileQ;
+        const int64_t t1 = imin(t0 + kTileQ, s.slot_q);
+        if (t0 >= t1) continue;
+        int64_t z0 = t0;  // first row to zero
+        bool accumulated = false, from_slots = false;
+        int64_t n_vis = 0;
+        if (t0 < s.len_q) {
+            int64_t first;
+            q_tile_visitors(g, s, j, first, n_vis);
+            if (n_vis > 0) z0 = s.len_q;
+            accumulated = n_vis >= 3 && !a.deterministic;
+            from_slots = n_vis >= 3 && a.deterministic && a.n_slots > 0;
         }
-    }
-    if (from_slots) {
-        // deterministic mode: the visitors' partials, summed in visitor order
+        auto dst_of = [&](int64_t i) {
+            return dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
+                   h * a.dq_stride[2] + c * 8;
+        };
         const int64_t e1 = imin(t1, s.len_q);
-        const int64_t nv = imin(n_vis, a.n_slots);
-        const float* base = a.dq_part + ((bi * g.h_q + h) * a.n_q_tiles + j) * a.n_slots * kTileQ * HD + c * 8;
-#pragma unroll 1
-        for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
-            const float* src = base + (i - t0) * HD;
-            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int64_t v = 0; v < nv; ++v) {
-                const float4 x = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[0];
-                const float4 y = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[1];
-                f[0] += x.x; f[1] += x.y; f[2] += x.z; f[3] += x.w;
-                f[4] += y.x; f[5] += y.y; f[6] += y.z; f[7] += y.w;
+        if (accumulated) {
+            // rows whose dQ was summed with unordered atomics: every row's loads
+            // issued before any conversion
+            float4 x[PASSES], y[PASSES];
+#pragma unroll
+            for (int k = 0; k < PASSES; ++k) {
+                const int64_t i = t0 + tid / TPR + k * RPP;
+                x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float* pf = a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8;
+                if (i < e1 && in_bounds(a.status, pf, a.dq_acc, g.ext.dq_acc, 8)) {
+                    const float4* src = reinterpret_cast<const float4*>(pf);
+                    x[k] = src[0];
+                    y[k] = src[1];
+                }
             }
-            uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
-                            h * a.dq_stride[2] + c * 8;
-            *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
+#pragma unroll
+            for (int k = 0; k < PASSES; ++k) {
+                const int64_t i = t0 + tid / TPR + k * RPP;
+                if (i < e1) {
+                    const float f[8] = {x[k].x, x[k].y, x[k].z, x[k].w, y[k].x, y[k].y, y[k].z, y[k].w};
+                    if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
+                        *reinterpret_cast<uint4*>(dst_of(i)) = pack8<BF16>(f);
+                }
+            }
         }
-    }
-    if (z0 >= t1) return;
+        if (from_slots) {
+            // deterministic mode: the visitors' partials, summed in visitor order
+            const int64_t nv = imin(n_vis, a.n_slots);
+            const float* base = a.dq_part + ((bi * g.h_q + h) * a.n_q_tiles + j) * a.n_slots * kTileQ * HD + c * 8;
 #pragma unroll 1
-    for (int64_t i = z0 + tid / TPR; i < t1; i += RPP) {
-        uint16_t* dst = dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
-                        h * a.dq_stride[2] + c * 8;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
+                const float* src = base + (i - t0) * HD;
+                float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int64_t v = 0; v < nv; ++v) {
+                    if (!in_bounds(a.status, src + v * kTileQ * HD, a.dq_part, g.ext.dq_part, 8)) continue;
+                    const float4 xv = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[0];
+                    const float4 yv = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[1];
+                    f[0] += xv.x; f[1] += xv.y; f[2] += xv.z; f[3] += xv.w;
+                    f[4] += yv.x; f[5] += yv.y; f[6] += yv.z; f[7] += yv.w;
+                }
+                if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
+                    *reinterpret_cast<uint4*>(dst_of(i)) = pack8<BF16>(f);
+            }
+        }
+        if (z0 >= t1) continue;
+#pragma unroll 1
+        for (int64_t i = z0 + tid / TPR; i < t1; i += RPP)
+            if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
+                *reinterpret_cast<uint4*>(dst_of(i)) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -359,9 +396,16 @@ cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
 
 cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s)
 {
-    const int64_t nx = (a.g.s_q + kTileQ - 1) / kTileQ;
-    if (nx == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(nx), static_cast<unsigned>(a.g.h_q), static_cast<unsigned>(a.g.b));
+    const int64_t tiles = a.n_q_tiles * a.g.h_q * a.g.b;
+    if (tiles == 0) return cudaSuccess;
+    if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // tiles are counted in 32 bits
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // eight 256-thread CTAs fit on an SM
+    const int64_t cap = int64_t(8) * sms;
+    const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
     SWA_DISPATCH(dq_convert_kernel, a, grid, s);
     return cudaGetLastError();
 }

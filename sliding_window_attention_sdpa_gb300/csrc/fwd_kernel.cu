@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kFThreads, 1) sdpa_fwd_kernel(const __grid_con
             }
             // Normaliser with the sink's term; LSE in natural log.
             float m_fin = m, l_tot = l;
-            if (a.sink != nullptr && valid) {
+            if (a.sink != nullptr && valid && in_bounds(a.status, a.sink + it.h, a.sink, g.ext.sink, 1)) {
                 const float sl = a.sink[it.h] * kLog2e;
                 if (m == -INFINITY) {
                     m_fin = sl;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kFThreads, 1) sdpa_fwd_kernel(const __grid_con
             const float lse = (valid && m_fin != -INFINITY) ? (m_fin + __log2f(l_tot)) * kLn2 : -INFINITY;
             if (in_slot) {
                 const int64_t so = thd ? it.h * g.rows_q + it.s.q_row0 + i : (it.bi * g.h_q + it.h) * g.s_q + i;
-                a.lse[so] = lse;
+                if (in_bounds(a.status, a.lse + so, a.lse, g.ext.lse, 1)) a.lse[so] = lse;
             }
             // O row: staged in the TMA layout (P's buffer), stored by TMA, or
             // row-wise for a THD tile that ends past its slot
@@ -523,9 +523,11 @@ __global__ void __launch_bounds__(kFThreads, 1) sdpa_fwd_kernel(const __grid_con
                 }
             } else if (in_slot) {
                 uint16_t* dst = static_cast<uint16_t*>(a.o) + (it.s.q_row0 + i) * a.o_stride[1] + it.h * a.o_stride[2];
+                if (in_bounds(a.status, dst, a.o, g.ext.o, HD)) {
 #pragma unroll
-                for (int cc = 0; cc < HD / 8; ++cc)
-                    *reinterpret_cast<uint4*>(dst + cc * 8) = *reinterpret_cast<const uint4*>(stg + fswz(r, cc));
+                    for (int cc = 0; cc < HD / 8; ++cc)
+                        *reinterpret_cast<uint4*>(dst + cc * 8) = *reinterpret_cast<const uint4*>(stg + fswz(r, cc));
+                }
             }
         }
     }
@@ -918,7 +920,7 @@ __global__ void __launch_bounds__(kPThreads, 1) sdpa_fwd_pp_kernel(const __grid_
             }
             // Normaliser with the sink's term; LSE in natural log.
             float m_fin = m, l_tot = l;
-            if (a.sink != nullptr && valid) {
+            if (a.sink != nullptr && valid && in_bounds(a.status, a.sink + it.h, a.sink, g.ext.sink, 1)) {
                 const float sk = a.sink[it.h] * kLog2e;
                 if (m == -INFINITY) {
                     m_fin = sk;
@@ -933,7 +935,7 @@ __global__ void __launch_bounds__(kPThreads, 1) sdpa_fwd_pp_kernel(const __grid_
             const float lse = (valid && m_fin != -INFINITY) ? (m_fin + __log2f(l_tot)) * kLn2 : -INFINITY;
             if (in_slot) {
                 const int64_t so = thd ? it.h * g.rows_q + it.s.q_row0 + i : (it.bi * g.h_q + it.h) * g.s_q + i;
-                a.lse[so] = lse;
+                if (in_bounds(a.status, a.lse + so, a.lse, g.ext.lse, 1)) a.lse[so] = lse;
             }
             // O row: staged in the TMA layout (P buffer 0), stored by TMA, or
             // row-wise for a THD tile that ends past its slot
@@ -974,9 +976,11 @@ __global__ void __launch_bounds__(kPThreads, 1) sdpa_fwd_pp_kernel(const __grid_
                 }
             } else if (in_slot) {
                 uint16_t* dst = static_cast<uint16_t*>(a.o) + (it.s.q_row0 + i) * a.o_stride[1] + it.h * a.o_stride[2];
+                if (in_bounds(a.status, dst, a.o, g.ext.o, HD)) {
 #pragma unroll
-                for (int cc = 0; cc < HD / 8; ++cc)
-                    *reinterpret_cast<uint4*>(dst + cc * 8) = *reinterpret_cast<const uint4*>(stg + fswz(r, cc));
+                    for (int cc = 0; cc < HD / 8; ++cc)
+                        *reinterpret_cast<uint4*>(dst + cc * 8) = *reinterpret_cast<const uint4*>(stg + fswz(r, cc));
+                }
             }
         }
     }

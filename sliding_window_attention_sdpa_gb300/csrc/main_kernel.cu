@@ -575,10 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                  (int)hh, qrow, (int)it.bi);
                     tma_tile<HD>(sbase + C::kDO + st * C::kTile, &a.tm_do, bar(kQFull0 + st), thd,
                                  (int)hh, qrow, (int)it.bi);
-                    bulk_load(sbase + C::kStat + st * 1024,
-                              a.stats + 2 * ((static_cast<int64_t>(it.bi) * g.h_q + hh) * a.stats_row +
-                                             static_cast<int64_t>(j) * kTileQ),
-                              1024, bar(kQFull0 + st));
+                    const float* srow = a.stats + 2 * ((static_cast<int64_t>(it.bi) * g.h_q + hh) * a.stats_row +
+                                                       static_cast<int64_t>(j) * kTileQ);
+                    if (in_bounds(a.status, srow, a.stats, g.ext.stats, 2 * kTileQ))
+                        bulk_load(sbase + C::kStat + st * 1024, srow, 1024, bar(kQFull0 + st));
                     SWA_TRACE(13, q_it);
                 }
                 if (!ok) break;
@@ -833,7 +833,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (have) w = *reinterpret_cast<const uint4*>(stg + stg_off(row, c));
                 uint16_t* dst = base + (thd ? (e.kv_row0 + kr) * sst[1] : e.bi * sst[0] + kr * sst[1]) +
                                 e.gk * sst[2] + c * 8;
-                *reinterpret_cast<uint4*>(dst) = w;
+                if (in_bounds(a.status, dst, base, half == 0 ? g.ext.dv : g.ext.dk, 8))
+                    *reinterpret_cast<uint4*>(dst) = w;
             }
         };
         // The next item's record is read right after this one's last P^T
@@ -1011,6 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 q_tile_visitors(g, it.s, j, first, nvis);
                 const int turn = static_cast<int>(it.t - first);
                 int32_t* sem = a.sems + (it.bi * g.h_q + hh) * a.n_q_tiles + j;
+                if (!in_bounds(a.status, sem, a.sems, g.ext.sems, 1)) sem = a.sems;
                 // TMA writes whole 128-row boxes: the tile must lie inside the
                 // sequence's slot (always so for BSHD, whose maps end at s_q)
                 const bool use_tma = !thd || (j + 1) * kTileQ <= it.s.slot_q;
@@ -1106,9 +1108,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         const float* accr =
                             a.dq_acc + ((it.s.q_row0 + (row_ok ? qi : it.s.len_q - 1)) * g.h_q + hh) * HD + ch * 32;
                         const float m = row_ok ? 1.f : 0.f;
+                        const bool acc_ok = in_bounds(a.status, accr, a.dq_acc, g.ext.dq_acc, 32);
 #pragma unroll
                         for (int e = 0; e < 32; e += 4) {
-                            const float4 o = ld_cg_f4(accr + e);
+                            const float4 o = acc_ok ? ld_cg_f4(accr + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                             f[e] += m * o.x; f[e + 1] += m * o.y; f[e + 2] += m * o.z; f[e + 3] += m * o.w;
                         }
                     }
@@ -1170,8 +1173,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                         if (conv_now && !single) {
                             float4 o[8];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                o[u] = ld_cg_f4((p0 + u) * 8 < nrows ? acc0 + (p0 + u) * acc_step : acc_last);
+                            for (int u = 0; u < 8; ++u) {
+                                const float* pl = (p0 + u) * 8 < nrows ? acc0 + (p0 + u) * acc_step : acc_last;
+                                o[u] = in_bounds(a.status, pl, a.dq_acc, g.ext.dq_acc, 4) ? ld_cg_f4(pl)
+                                                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
 #pragma unroll
                             for (int u = 0; u < 8; ++u) {
                                 v[u].x += o[u].x; v[u].y += o[u].y; v[u].z += o[u].z; v[u].w += o[u].w;
@@ -1187,8 +1193,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                                 (thd ? prow * a.dq_stride[1]
                                                      : it.bi * a.dq_stride[0] + qi * a.dq_stride[1]) +
                                                 hh * a.dq_stride[2] + col;
-                                *reinterpret_cast<uint2*>(dqp) =
-                                    make_uint2(pack2<BF16>(v[u].x, v[u].y), pack2<BF16>(v[u].z, v[u].w));
+                                if (in_bounds(a.status, dqp, a.dq, g.ext.dq, 4))
+                                    *reinterpret_cast<uint2*>(dqp) =
+                                        make_uint2(pack2<BF16>(v[u].x, v[u].y), pack2<BF16>(v[u].z, v[u].w));
+                            } else if (!in_bounds(a.status, accp, a.dq_acc, g.ext.dq_acc, 4)) {
                             } else if (!add) {
                                 *reinterpret_cast<float4*>(accp) = v[u];
                             } else {

@@ -32,6 +32,7 @@ constexpr size_t kItemBytes = 152;
 constexpr int kStatusUnsupported = 2;  // same codes as sdpa_status_t
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadLengths = 5;
+constexpr int kStatusBounds = 7;     // range-checked build: an access fell outside its buffer
 // Second status word: which global-memory wait of the main kernel ran out
 // first (0: none, or an mbarrier hand-off inside a CTA).
 constexpr int kWhereRelay = 200;   // a relay turn
@@ -57,6 +58,16 @@ struct WsLayout {
     int64_t n_row_blocks;
 };
 
+// Elements reachable from each base pointer, for the range-checked build
+// (-DSDPA_DEBUG_BOUNDS): every raw global access checks its index against
+// these, records kStatusBounds and skips the access if it falls outside.
+// Unused (and the checks compiled out) otherwise.
+struct Extents {
+    int64_t q, k, v, o, dout, dq, dk, dv;   // 16-bit elements
+    int64_t lse, stats, dq_acc, dq_part, dsink_part, sink;   // fp32 elements
+    int64_t sems;                           // int32 counters
+};
+
 // Sequence geometry common to all kernels.
 struct Geometry {
     int32_t layout;     // 0 BSHD, 1 THD
@@ -69,6 +80,7 @@ struct Geometry {
     const int32_t* seq_kv_lens;
     const int32_t* q_offsets;
     const int32_t* kv_offsets;
+    Extents ext;
 };
 
 struct PreArgs {
@@ -157,6 +169,7 @@ struct CvtArgs {
     const float* dsink_part;
     int64_t n_row_blocks;
     float* dsink;
+    int32_t* status;      // device status word (range-checked build)
 };
 
 // The forward pass (O and LSE): one work item per (q-tile, q-head, sequence).

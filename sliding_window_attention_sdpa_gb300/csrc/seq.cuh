@@ -75,6 +75,25 @@ __device__ __forceinline__ void set_status(int32_t* status, int code)
     atomicCAS(status, 0, code);
 }
 
+// Range-checked build (-DSDPA_DEBUG_BOUNDS): true if elements [p, p + count)
+// lie inside [base, base + extent); otherwise records kStatusBounds and
+// returns false so that the caller skips the access. Always true otherwise.
+template <typename T>
+__device__ __forceinline__ bool in_bounds(int32_t* status, const T* p, const void* base, int64_t extent,
+                                          int64_t count)
+{
+#ifdef SDPA_DEBUG_BOUNDS
+    const int64_t off = p - static_cast<const T*>(base);
+    if (off < 0 || off + count > extent) {
+        set_status(status, kStatusBounds);
+        return false;
+    }
+#else
+    (void)status; (void)p; (void)base; (void)extent; (void)count;
+#endif
+    return true;
+}
+
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
 
