@@ -63,7 +63,13 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
 // register path (address arithmetic per 16 bytes, cross-thread reductions)
 // made it issue-bound at about half the HBM bandwidth. Every row of every
 // q-tile is covered: rows past the length get the statistics that make P = 0.
-constexpr uint32_t kPreRing = 196608;   // bytes of the ring: stages of an O box and a dO box
+// Bytes of the ring (stages of an O box and a dO box): 192 KB with one CTA
+// per SM, 64 KB with three. Three CTAs of two stages each keep as many bytes in
+// flight as one CTA of six, and one CTA's wait-reduce-reissue turn overlaps the
+// others' (THD b16 h64: 201 us against 258; b2 h16 S8192: 16.6 against
+// 18.9 us). Small problems (fewer than four blocks per CTA at three per SM)
+// keep one CTA per SM.
+constexpr uint32_t kPreRingOne = 196608, kPreRingThree = 65536;
 constexpr int kPreMaxStages = 8;
 
 __device__ __forceinline__ void pre_tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool thd,
@@ -84,18 +90,19 @@ __device__ __forceinline__ void pre_tma_load(uint32_t dst, const CUtensorMap* ma
 }
 
 template <int HD, bool BF16>
-__global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constant__ PreArgs a)
+__global__ void __launch_bounds__(256, 3) preprocess_kernel(const __grid_constant__ PreArgs a)
 {
     constexpr int TPU = HD / 64;   // threads per (row, head) unit, 128 B each
     extern __shared__ __align__(1024) uint8_t smem[];
     // [stage][O box | dO box], dSink row terms [2][256] fp32, mbarriers
-    float* red = reinterpret_cast<float*>(smem + kPreRing);
+    const uint32_t ring = a.ring_bytes;
+    float* red = reinterpret_cast<float*>(smem + ring);
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 127u) {   // TMA destinations need 128-byte alignment
         if (threadIdx.x == 0) set_status(a.status, kStatusUnsupported);
         return;
     }
-    const uint32_t bars = sbase + kPreRing + 2 * 256 * 4;
+    const uint32_t bars = sbase + ring + 2 * 256 * 4;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
     const bool thd = g.layout == 1;
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
     const uint32_t n_items = static_cast<uint32_t>(g.b) * nrb * nhc;
     // as many ring stages as boxes of this size fit
     const uint32_t stage_bytes = 2 * box_bytes;
-    const int n_stages = static_cast<int>(min(kPreRing / stage_bytes, static_cast<uint32_t>(kPreMaxStages)));
+    const int n_stages = static_cast<int>(min(ring / stage_bytes, static_cast<uint32_t>(kPreMaxStages)));
 
     // relay / visit counters, ticket and status: zeroed by the whole grid
     {
@@ -252,42 +259,66 @@ __global__ void __launch_bounds__(256, 1) preprocess_kernel(const __grid_constan
 // rows past the sequence's length and q-tiles no kv-tile visits; converts the
 // q-tiles whose visitors added with unordered atomics, and sums (in visitor
 // order) and converts those whose visitors stored per-visitor partials. It
-// also finishes dSink in a fixed order. Persistent: CTA c walks the
-// (q-head, q-tile, sequence) tiles c, c + grid, ..., head fastest (one
-// [row][head][d] row holds every head), so that a grid of a few waves covers
-// problems whose tiles mostly need nothing.
+// also finishes dSink in a fixed order.
+// Persistent: CTA c walks the units c, c + grid, ... of (sequence, q-tile,
+// chunk of head_chunk q-heads), chunk fastest. A unit reads its sequence's
+// lengths and visitor run once and then moves all of its (row, head) pieces
+// as one flat, coalesced range ([row][head][d] rows hold every head side by
+// side), four 32-byte loads in flight per thread.
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
 {
-    constexpr int TPR = HD / 8;         // threads per row (8 values each)
-    constexpr int RPP = 256 / TPR;      // rows per pass
-    constexpr int PASSES = kTileQ / RPP;
+    constexpr int TPR = HD / 8;         // threads per (row, head): 8 values each
+    constexpr int kBatch = 4;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
-    const int c = tid % TPR;
-    if (a.dsink != nullptr && blockIdx.x == 0) {
-        // fixed-order finish, a warp per head: lane l sums partials l, l + 32,
-        // ... in order, then a fixed butterfly; bitwise repeatable
-        const int lane = tid & 31;
-        for (int64_t hh = tid >> 5; hh < g.h_q; hh += blockDim.x >> 5) {
+    if (a.dsink != nullptr) {
+        // fixed-order finish, one CTA per head: thread t sums partials t,
+        // t + 256, ... in order (eight loads in flight at a time), then a fixed
+        // butterfly in each warp and the eight warp sums in warp order; bitwise
+        // repeatable for a given problem
+        __shared__ float wsum[8];
+        const int lane = tid & 31, wid = tid >> 5;
+        for (int64_t hh = blockIdx.x; hh < g.h_q; hh += gridDim.x) {
+            const float* src = a.dsink_part + hh * a.n_row_blocks;
             float t = 0.f;
-            for (int64_t k = lane; k < a.n_row_blocks; k += 32)
-                if (in_bounds(a.status, a.dsink_part + hh * a.n_row_blocks + k, a.dsink_part, g.ext.dsink_part, 1))
-                    t += a.dsink_part[hh * a.n_row_blocks + k];
+#pragma unroll 1
+            for (int64_t k0 = tid; k0 < a.n_row_blocks; k0 += 8 * 256) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int64_t k = k0 + q * 256;
+                    v[q] = (k < a.n_row_blocks && in_bounds(a.status, src + k, a.dsink_part, g.ext.dsink_part, 1))
+                               ? src[k] : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) t += v[q];
+            }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-            if (lane == 0) a.dsink[hh] = t;
+            if (lane == 0) wsum[wid] = t;
+            __syncthreads();
+            if (tid == 0) {
+                float s = 0.f;
+                for (int w = 0; w < 8; ++w) s += wsum[w];
+                a.dsink[hh] = s;
+            }
+            __syncthreads();
         }
     }
     const bool thd = g.layout == 1;
     uint16_t* dq = static_cast<uint16_t*>(a.dq);
     const uint32_t hq = static_cast<uint32_t>(g.h_q), nx = static_cast<uint32_t>(a.n_q_tiles);
-    const uint32_t n_tiles = hq * nx * static_cast<uint32_t>(g.b);
-    for (uint32_t u = blockIdx.x; u < n_tiles; u += gridDim.x) {
-        const uint32_t rest = u / hq, bq = rest / nx;
-        const int64_t h = u - rest * hq, j = rest - bq * nx, bi = bq;
+    const uint32_t hc = static_cast<uint32_t>(a.head_chunk);
+    const uint32_t nhc = (hq + hc - 1) / hc;
+    const uint32_t n_units = nhc * nx * static_cast<uint32_t>(g.b);
+    for (uint32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const uint32_t rest = u / nhc, bq = rest / nx;
+        const uint32_t h0 = (u - rest * nhc) * hc, j = rest - bq * nx;
+        const uint32_t nh = min(hc, hq - h0);
+        const int64_t bi = bq;
         const SeqInfo s = seq_info(g, bi);
-        const int64_t t0 = j * kTileQ;
+        const int64_t t0 = static_cast<int64_t>(j) * kTileQ;
         const int64_t t1 = imin(t0 + kTileQ, s.slot_q);
         if (t0 >= t1) continue;
         int64_t z0 = t0;  // first row to zero
@@ -300,43 +331,52 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
             accumulated = n_vis >= 3 && !a.deterministic;
             from_slots = n_vis >= 3 && a.deterministic && a.n_slots > 0;
         }
-        auto dst_of = [&](int64_t i) {
-            return dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
-                   h * a.dq_stride[2] + c * 8;
-        };
         const int64_t e1 = imin(t1, s.len_q);
+        const uint32_t per_row = nh * TPR;   // pieces of one row
+        // piece k of rows [r0, ...): row r0 + k / per_row, head h0 + (k / TPR) % nh, column block k % TPR
+        auto dst_of = [&](int64_t i, uint32_t h, uint32_t c) {
+            return dq + (thd ? (s.q_row0 + i) * a.dq_stride[1] : bi * a.dq_stride[0] + i * a.dq_stride[1]) +
+                   static_cast<int64_t>(h) * a.dq_stride[2] + c * 8;
+        };
         if (accumulated) {
-            // rows whose dQ was summed with unordered atomics: every row's loads
-            // issued before any conversion
-            float4 x[PASSES], y[PASSES];
+            // rows whose dQ was summed with unordered atomics
+            const uint32_t n = static_cast<uint32_t>(e1 - t0) * per_row;
+#pragma unroll 1
+            for (uint32_t k0 = tid; k0 < n; k0 += kBatch * 256) {
+                float4 x[kBatch], y[kBatch];
 #pragma unroll
-            for (int k = 0; k < PASSES; ++k) {
-                const int64_t i = t0 + tid / TPR + k * RPP;
-                x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float* pf = a.dq_acc + ((s.q_row0 + i) * g.h_q + h) * HD + c * 8;
-                if (i < e1 && in_bounds(a.status, pf, a.dq_acc, g.ext.dq_acc, 8)) {
-                    const float4* src = reinterpret_cast<const float4*>(pf);
-                    x[k] = src[0];
-                    y[k] = src[1];
+                for (int q = 0; q < kBatch; ++q) {
+                    const uint32_t k = k0 + q * 256;
+                    x[q] = y[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const uint32_t r = k / per_row, rem = k - r * per_row;
+                    const float* pf = a.dq_acc + ((s.q_row0 + t0 + r) * g.h_q + h0) * HD + rem * 8;
+                    if (k < n && in_bounds(a.status, pf, a.dq_acc, g.ext.dq_acc, 8)) {
+                        const float4* src = reinterpret_cast<const float4*>(pf);
+                        x[q] = src[0];
+                        y[q] = src[1];
+                    }
                 }
-            }
 #pragma unroll
-            for (int k = 0; k < PASSES; ++k) {
-                const int64_t i = t0 + tid / TPR + k * RPP;
-                if (i < e1) {
-                    const float f[8] = {x[k].x, x[k].y, x[k].z, x[k].w, y[k].x, y[k].y, y[k].z, y[k].w};
-                    if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
-                        *reinterpret_cast<uint4*>(dst_of(i)) = pack8<BF16>(f);
+                for (int q = 0; q < kBatch; ++q) {
+                    const uint32_t k = k0 + q * 256;
+                    if (k >= n) break;
+                    const uint32_t r = k / per_row, rem = k - r * per_row, hl = rem / TPR;
+                    uint16_t* dst = dst_of(t0 + r, h0 + hl, rem - hl * TPR);
+                    const float f[8] = {x[q].x, x[q].y, x[q].z, x[q].w, y[q].x, y[q].y, y[q].z, y[q].w};
+                    if (in_bounds(a.status, dst, a.dq, g.ext.dq, 8))
+                        *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
                 }
             }
         }
         if (from_slots) {
             // deterministic mode: the visitors' partials, summed in visitor order
             const int64_t nv = imin(n_vis, a.n_slots);
-            const float* base = a.dq_part + ((bi * g.h_q + h) * a.n_q_tiles + j) * a.n_slots * kTileQ * HD + c * 8;
+            const uint32_t n = static_cast<uint32_t>(e1 - t0) * per_row;
 #pragma unroll 1
-            for (int64_t i = t0 + tid / TPR; i < e1; i += RPP) {
-                const float* src = base + (i - t0) * HD;
+            for (uint32_t k = tid; k < n; k += 256) {
+                const uint32_t r = k / per_row, rem = k - r * per_row, hl = rem / TPR, c = rem - hl * TPR;
+                const float* src = a.dq_part +
+                                   (((bi * g.h_q + h0 + hl) * a.n_q_tiles + j) * a.n_slots * kTileQ + r) * HD + c * 8;
                 float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int64_t v = 0; v < nv; ++v) {
@@ -346,15 +386,19 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
                     f[0] += xv.x; f[1] += xv.y; f[2] += xv.z; f[3] += xv.w;
                     f[4] += yv.x; f[5] += yv.y; f[6] += yv.z; f[7] += yv.w;
                 }
-                if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
-                    *reinterpret_cast<uint4*>(dst_of(i)) = pack8<BF16>(f);
+                uint16_t* dst = dst_of(t0 + r, h0 + hl, c);
+                if (in_bounds(a.status, dst, a.dq, g.ext.dq, 8))
+                    *reinterpret_cast<uint4*>(dst) = pack8<BF16>(f);
             }
         }
         if (z0 >= t1) continue;
+        const uint32_t n = static_cast<uint32_t>(t1 - z0) * per_row;
 #pragma unroll 1
-        for (int64_t i = z0 + tid / TPR; i < t1; i += RPP)
-            if (in_bounds(a.status, dst_of(i), a.dq, g.ext.dq, 8))
-                *reinterpret_cast<uint4*>(dst_of(i)) = make_uint4(0u, 0u, 0u, 0u);
+        for (uint32_t k = tid; k < n; k += 256) {
+            const uint32_t r = k / per_row, rem = k - r * per_row, hl = rem / TPR;
+            uint16_t* dst = dst_of(z0 + r, h0 + hl, rem - hl * TPR);
+            if (in_bounds(a.status, dst, a.dq, g.ext.dq, 8)) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -368,8 +412,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
         else KERNEL<128, false><<<GRID, 256, 0, STREAM>>>(ARGS);                           \
     } while (0)
 
-cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
+cudaError_t launch_preprocess(const PreArgs& a_in, int dtype, cudaStream_t s)
 {
+    PreArgs a = a_in;
     if (a.stats_row == 0 || a.g.b == 0 || a.g.h_q == 0) return cudaSuccess;
     const int64_t items = a.g.b * (a.stats_row / a.pre_rows) * ((a.g.h_q + a.pre_heads - 1) / a.pre_heads);
     if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // blocks are counted in 32 bits
@@ -377,8 +422,11 @@ cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-    const size_t smem = kPreRing + 2 * 256 * 4 + 8 * kPreMaxStages;
+    const bool three = items >= int64_t(4) * 3 * sms;
+    a.ring_bytes = three ? kPreRingThree : kPreRingOne;
+    const int64_t cap = three ? int64_t(3) * sms : sms;
+    const unsigned grid = static_cast<unsigned>(items < cap ? items : cap);
+    const size_t smem = a.ring_bytes + 2 * 256 * 4 + 8 * kPreMaxStages;
 #define SWA_PRE(HD, BF)                                                                                   \
     do {                                                                                                  \
         if ((e = cudaFuncSetAttribute(preprocess_kernel<HD, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
@@ -394,18 +442,25 @@ cudaError_t launch_preprocess(const PreArgs& a, int dtype, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const CvtArgs& a, int dtype, cudaStream_t s)
+cudaError_t launch_dq_convert(const CvtArgs& a_in, int dtype, cudaStream_t s)
 {
-    const int64_t tiles = a.n_q_tiles * a.g.h_q * a.g.b;
-    if (tiles == 0) return cudaSuccess;
-    if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // tiles are counted in 32 bits
+    CvtArgs a = a_in;
+    const int64_t n_bj = a.n_q_tiles * a.g.b;
+    if (n_bj == 0 || a.g.h_q == 0) return cudaSuccess;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // heads per unit: as many as keep at least two units per SM
+    int64_t hc = a.g.h_q * n_bj / (2 * static_cast<int64_t>(sms));
+    hc = hc < 1 ? 1 : (hc > a.g.h_q ? a.g.h_q : hc);
+    a.head_chunk = static_cast<int32_t>(hc);
+    const int64_t units = n_bj * ((a.g.h_q + hc - 1) / hc);
+    if (units >= (int64_t(1) << 31) || 128 * a.g.h_q * (a.g.d / 8) >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;   // units and pieces are counted in 32 bits
     // eight 256-thread CTAs fit on an SM
     const int64_t cap = int64_t(8) * sms;
-    const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
+    const unsigned grid = static_cast<unsigned>(units < cap ? units : cap);
     SWA_DISPATCH(dq_convert_kernel, a, grid, s);
     return cudaGetLastError();
 }

@@ -107,6 +107,7 @@ struct PreArgs {
     int64_t n_sems;
     float* dsink_part;
     int64_t n_row_blocks;
+    uint32_t ring_bytes;  // shared-memory ring of O/dO stages (set by the launcher)
 };
 
 struct MainArgs {
@@ -170,6 +171,7 @@ struct CvtArgs {
     int64_t n_row_blocks;
     float* dsink;
     int32_t* status;      // device status word (range-checked build)
+    int32_t head_chunk;   // q-heads per unit (set by the launcher)
 };
 
 // The forward pass (O and LSE): one work item per (q-tile, q-head, sequence).
