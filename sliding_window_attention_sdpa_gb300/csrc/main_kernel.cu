@@ -105,6 +105,12 @@ struct Cfg {
     static constexpr uint32_t kColDQ = HD == 64 ? 384 : 0;
     static constexpr uint32_t kColP = 448;                      // d = 64 only
     static constexpr bool kDqAliasesS = HD != 64;
+    // d = 64: the dQ warps write each item's dK/dV, staged in the item's own
+    // K/V ring entry (idle once its last contractions are done), and hand the
+    // entry back to the producer when their stores have read it. The softmax
+    // group then runs its q-tiles back to back across items. At d = 128 the
+    // softmax group writes them, staged in its P^T and dS^T buffers.
+    static constexpr bool kEpiDq = HD == 64;
     static_assert(!(kAhead && kDqAliasesS), "look-ahead overwrites S^T while dQ would alias it");
 };
 
@@ -294,6 +300,9 @@ struct Item {
     int64_t nq, steps;   // q-tiles per head, steps = group * nq
     bool has_work;       // at least one q-tile to sweep
     bool in_slot;        // the kv-tile has rows inside the sequence's slot
+    // strip mode: tmem_pair() of the first and the last step (the only steps
+    // that can pair when a q-tile has at most two visitors), set by with_pairs
+    uint8_t tp_first, tp_last;
     // Steps run q-head h0 .. h0 + group - 1, each over its q-tiles from q_hi - 1
     // down to q_lo, or (strip mode, UP) from q_lo up to q_hi - 1; counters
     // rather than divisions (there is no 64-bit divider, and these sit on every
@@ -417,6 +426,19 @@ __device__ __forceinline__ int tmem_pair(const Geometry& g, const Item& it, int6
     }
 }
 
+// An item with its first and last steps' tmem_pair() filled in (once per
+// item, instead of the visitor arithmetic at every step of the MMA warp).
+template <bool STRIP>
+__device__ __forceinline__ Item with_pairs(const Geometry& g, Item it, int64_t item, const Walk& wk)
+{
+    it.tp_first = it.tp_last = 0;
+    if (STRIP && it.has_work && it.group == 1) {
+        it.tp_first = static_cast<uint8_t>(tmem_pair<STRIP>(g, it, it.template first_j<STRIP>(), item, wk));
+        it.tp_last = static_cast<uint8_t>(tmem_pair<STRIP>(g, it, STRIP ? it.q_hi - 1 : it.q_lo, item, wk));
+    }
+    return it;
+}
+
 // Zeroes rows [nvalid, 128) of a swizzled tile (whole 128-byte rows, so the
 // swizzle does not matter); run by one warp, then made visible to the tensor
 // core. Used where rows past a sequence end hold data of another sequence
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         mbar_init(bar(kDqFull), 1);
         mbar_init(bar(kDqEmpty), 128);
         mbar_init(bar(kAccFull), 1);
-        mbar_init(bar(kAccEmpty), kSoftThreads);
+        mbar_init(bar(kAccEmpty), C::kEpiDq ? 128 : kSoftThreads);
         mbar_init(bar(kDqLoad), 1);
         mbar_init(bar(kDrain), 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -514,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     if (use_items)
         for (int64_t item = wk.begin + static_cast<int64_t>(tid) * wk.stride; item < wk.end;
              item += static_cast<int64_t>(kThreads) * wk.stride)
-            items[item] = decode<STRIP>(a, cnt, item);
+            items[item] = with_pairs<STRIP>(g, decode<STRIP>(a, cnt, item), item, wk);
     auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode<STRIP>(a, cnt, i); };
     tc_fence_before();
     __syncthreads();   // also publishes the item table to the CTA
@@ -609,38 +631,56 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             int tpair;                // tmem_pair() of the step
         };
         Pending pend{false, false, false, 0, 0, 0u, 0};
+        // Operand descriptors of ring entry 0 and dS^T buffer 0; other entries
+        // are a byte offset away (sdesc_at). K-major (16, 1024) for S^T, dP^T
+        // and the dK A operand; MN-major (16 KB, 1024) for the B operands of
+        // dV, dK and the operands of dQ.
+        const uint64_t dK0 = sdesc_sw128(sbase + C::kK, 16, 1024), dV0 = sdesc_sw128(sbase + C::kV, 16, 1024);
+        const uint64_t dQ0 = sdesc_sw128(sbase + C::kQ, 16, 1024), dDO0 = sdesc_sw128(sbase + C::kDO, 16, 1024);
+        const uint64_t dDOmn0 = sdesc_sw128(sbase + C::kDO, kBlock16K, 1024);
+        const uint64_t dQmn0 = sdesc_sw128(sbase + C::kQ, kBlock16K, 1024);
+        const uint64_t dKmn0 = sdesc_sw128(sbase + C::kK, kBlock16K, 1024);
+        const uint64_t dDSk0 = sdesc_sw128(sbase + C::kDS, 16, 1024);
+        const uint64_t dDSmn0 = sdesc_sw128(sbase + C::kDS, kBlock16K, 1024);
         // dV += P^T dO, dK += dS^T Q, dQ = dS K for step `p` (softmax done).
         auto issue_grads = [&](const Pending& p) -> bool {
             if (p.first && !wait_warp(kAccEmpty, (acc_it & 1) ^ 1)) return false;
-            const uint32_t sK = sbase + C::kK + p.ks * C::kTile;
-            const uint32_t sQ = sbase + C::kQ + p.st * C::kTile, sDO = sbase + C::kDO + p.st * C::kTile;
-            const uint32_t sDS = sbase + C::kDS + (p.q_it % C::kDsBufs) * 32768u;
+            const uint32_t kv_off = p.ks * C::kTile, q_off = p.st * C::kTile;
+            const uint32_t ds_off = (p.q_it % C::kDsBufs) * 32768u;
             {
                 SWA_TRACE(3, p.q_it);
                 tc_fence_after();
                 const uint32_t acc = p.first ? 0u : 1u;
                 // K-major (16, 1024) and MN-major (16 KB, 1024) descriptors of the
                 // operand tiles; each contraction step adds its byte offset
-                const uint64_t dDOmn = sdesc_sw128(sDO, kBlock16K, 1024), dQmn = sdesc_sw128(sQ, kBlock16K, 1024);
-                const uint64_t dDSk = sdesc_sw128(sDS, 16, 1024);
+                const uint64_t dDOmn = sdesc_at(dDOmn0, q_off), dQmn = sdesc_at(dQmn0, q_off);
+                const uint64_t dDSk = sdesc_at(dDSk0, ds_off);
+                if constexpr (C::kPInTmem) {
+                    // contraction step k: P^T columns 8 k, dO rows 16 k (2 KB)
+                    umma_f16_ts_x4(tm_dv, tmem + C::kColP, 8, dDOmn, 2048 >> 4, kIdPV, acc);
+                    umma_f16_ts_x4(tm_dv, tmem + C::kColP + 32, 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t bdesc = sdesc_at(dDOmn, k * 2048);
-                    if constexpr (C::kPInTmem) {
-                        umma_f16_ts(tm_dv, tmem + C::kColP + k * 8, bdesc, kIdPV, acc | (k > 0));
-                    } else {
+                    for (int k = 0; k < 8; ++k) {
                         const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), bdesc, kIdPV,
-                                    acc | (k > 0));
+                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), sdesc_at(dDOmn, k * 2048),
+                                    kIdPV, acc | (k > 0));
                     }
                 }
                 // P^T is free (and, with everything issued before, the dS^T
                 // buffer of the step before this one)
                 if constexpr (C::kAhead) umma_commit(bar(kPEmpty));
+                if constexpr (C::kAhead) {
+                    // dS^T columns 16 k (32 bytes, then the next 16 KB block), Q rows 16 k
+                    umma_f16_ss_x4(tm_dk, dDSk, 32 >> 4, dQmn, 2048 >> 4, kIdPV, acc);
+                    umma_f16_ss_x4(tm_dk, sdesc_at(dDSk, kBlock16K), 32 >> 4, sdesc_at(dQmn, 4 * 2048), 2048 >> 4,
+                                   kIdPV, 1);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                    umma_f16_ss(tm_dk, sdesc_at(dDSk, aoff), sdesc_at(dQmn, k * 2048), kIdPV, acc | (k > 0));
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                        umma_f16_ss(tm_dk, sdesc_at(dDSk, aoff), sdesc_at(dQmn, k * 2048), kIdPV, acc | (k > 0));
+                    }
                 }
                 // Q and dO have been read (dQ below reads only dS and K): the
                 // stage goes back to the producer
@@ -657,16 +697,26 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             }
             {
                 tc_fence_after();
-                const uint64_t dKmn = sdesc_sw128(sK, kBlock16K, 1024), dDSmn = sdesc_sw128(sDS, kBlock16K, 1024);
+                const uint64_t dKmn = sdesc_at(dKmn0, kv_off), dDSmn = sdesc_at(dDSmn0, ds_off);
+                if constexpr (C::kAhead) {
+                    // dS rows and K rows 16 k (2 KB each)
+                    umma_f16_ss_x4(tm_dq, dDSmn, 2048 >> 4, dKmn, 2048 >> 4, kIdDQ, dq_onto);
+                    umma_f16_ss_x4(tm_dq, sdesc_at(dDSmn, 4 * 2048), 2048 >> 4, sdesc_at(dKmn, 4 * 2048), 2048 >> 4,
+                                   kIdDQ, 1);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ, k > 0 || dq_onto);
+                    for (int k = 0; k < 8; ++k)
+                        umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ,
+                                    k > 0 || dq_onto);
+                }
                 if (p.tpair != 1) umma_commit(bar(kDqFull));
                 SWA_TRACE(4, p.q_it);
                 if (p.last) {
-                    // after dQ: the epilogue stages dK/dV in this step's dS^T buffer
+                    // after dQ: the epilogue stages dK/dV in this step's dS^T
+                    // buffer (d = 128) or in this item's K/V entry (d = 64, whose
+                    // epilogue releases the entry)
                     umma_commit(bar(kAccFull));
-                    umma_commit(bar(kKvEmpty0 + p.ks));
+                    if constexpr (!C::kEpiDq) umma_commit(bar(kKvEmpty0 + p.ks));
                 }
             }
             __syncwarp();
@@ -675,12 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         bool ok = true;
         for (int64_t item = wk.begin; item < wk.end && ok; item += wk.stride) {
-            const Item it = item_at(item);
+            const Item it = use_items ? items[item] : with_pairs<STRIP>(g, item_at(item), item, wk);
             if (!it.has_work) continue;
             const int ks = kv_it % C::kKvStages;
             if (!(ok = wait_warp(kKvFull0 + ks, (kv_it / C::kKvStages) & 1))) break;
             ++kv_it;
-            const uint32_t sK = sbase + C::kK + ks * C::kTile, sV = sbase + C::kV + ks * C::kTile;
             if (it.kv_base + kTileKV > it.s.len_kv)
                 zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
             for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
@@ -692,6 +741,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     zero_tail<HD>(sm + C::kQ + st * C::kTile, it.s.len_q - q0, lane);
                     zero_tail<HD>(sm + C::kDO + st * C::kTile, it.s.len_q - q0, lane);
                 }
+                // this step's bookkeeping and operand descriptors, ahead of the
+                // wait for the softmax
+                const int tp = it.steps <= 2 ? (k == 0 ? it.tp_first : it.tp_last) : tmem_pair<STRIP>(g, it, j, item, wk);
+                const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it, tp};
+                const uint64_t dK = sdesc_at(dK0, ks * C::kTile), dQ = sdesc_at(dQ0, st * C::kTile);
+                const uint64_t dV = sdesc_at(dV0, ks * C::kTile), dDO = sdesc_at(dDO0, st * C::kTile);
                 if (C::kAhead && pend.valid) {
                     // P^T, dS^T of the pending step are written and the softmax
                     // is done with S^T, dP^T
@@ -701,26 +756,28 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 }
                 // S^T and dP^T overwrite TMEM that the previous dQ may alias
                 if (C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
-                const uint32_t sQ = sbase + C::kQ + st * C::kTile, sDO = sbase + C::kDO + st * C::kTile;
                 {
                     tc_fence_after();
-                    const uint64_t dK = sdesc_sw128(sK, 16, 1024), dQ = sdesc_sw128(sQ, 16, 1024);
-                    const uint64_t dV = sdesc_sw128(sV, 16, 1024), dDO = sdesc_sw128(sDO, 16, 1024);
+                    if constexpr (HD == 64) {
+                        // contraction step k: 32 bytes into the rows of K, Q, V, dO
+                        umma_f16_ss_x4(tm_s, dK, 32 >> 4, dQ, 32 >> 4, kIdQK, 0);
+                        umma_f16_ss_x4(tm_dp, dV, 32 >> 4, dDO, 32 >> 4, kIdQK, 0);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < HD / 16; ++k) {
-                        const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_s, sdesc_at(dK, koff), sdesc_at(dQ, koff), kIdQK, k > 0);
-                    }
+                        for (int k = 0; k < HD / 16; ++k) {
+                            const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                            umma_f16_ss(tm_s, sdesc_at(dK, koff), sdesc_at(dQ, koff), kIdQK, k > 0);
+                        }
 #pragma unroll
-                    for (int k = 0; k < HD / 16; ++k) {
-                        const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dp, sdesc_at(dV, koff), sdesc_at(dDO, koff), kIdQK, k > 0);
+                        for (int k = 0; k < HD / 16; ++k) {
+                            const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
+                            umma_f16_ss(tm_dp, sdesc_at(dV, koff), sdesc_at(dDO, koff), kIdQK, k > 0);
+                        }
                     }
                     umma_commit(bar(kSFull));
                     SWA_TRACE(1, q_it);
                 }
                 __syncwarp();
-                const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it, tmem_pair<STRIP>(g, it, j, item, wk)};
                 if constexpr (C::kAhead) {
                     if (pend.valid && !(ok = issue_grads(pend))) break;
                     pend = cur;
@@ -855,7 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(20, q_it);
-                    release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
+                    if constexpr (!C::kEpiDq)
+                        release_buf(static_cast<int>(q_it % C::kDsBufs));   // ordered by the barrier below
                     if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(21, q_it);
                     // this q-tile's (LSE, D) pairs and S^T, dP^T: one group barrier
                     if (!(ok = bar_and(kBarSoft, kSoftThreads,
@@ -951,16 +1009,18 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     mbar_arrive(bar(kPFull));
                     if (lane == 0 && (warp == kWarpSoft0 || warp == kWarpSoft0 + 4))
                         SWA_TRACE(warp == kWarpSoft0 ? 6 : 8, q_it);
-                    if (epi_pending) {
-                        // the previous item's dK/dV store, deferred to here
-                        epi_pending = false;
-                        run_epi(*epi_slot);
+                    if constexpr (!C::kEpiDq) {
+                        if (epi_pending) {
+                            // the previous item's dK/dV store, deferred to here
+                            epi_pending = false;
+                            run_epi(*epi_slot);
+                        }
                     }
                 }
                 nxt = decode_at(item + wk.stride);
                 have_nxt = true;
             }
-            if (!it.in_slot) continue;
+            if (C::kEpiDq || !it.in_slot) continue;   // d = 64: the dQ warps write dK/dV
             const Epi e{it.kv_base, it.s.kv_row0, it.s.len_kv, it.s.slot_kv, it.bi, it.gk, acc_it & 1,
                         static_cast<int32_t>((q_it + C::kDsBufs - 1) % C::kDsBufs),
                         static_cast<int32_t>(it.has_work && ok), static_cast<int32_t>(q_it - 1)};
@@ -975,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 run_epi(e);
             }
         }
-        if (epi_pending) {
+        if (!C::kEpiDq && epi_pending) {
             named_bar_sync(kBarSoft, kSoftThreads);   // epi_slot's write is visible
             run_epi(*epi_slot);
         }
@@ -1002,9 +1062,118 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const uint32_t stg_s = sbase + C::kDqStage;
         uint32_t dq_it = 0, ld_it = 0;
         bool ok = true;
+        // d = 64 dK/dV epilogue state: K/V ring entry an issued store may still
+        // be reading (-1: none), and the counters of items with work (their
+        // K/V entry and accumulator phase, as the producer and MMA count them)
+        int kv_pend = -1;
+        uint32_t ekv_it = 0, eacc_it = 0;
+        // The entry goes back to the producer once thread 0's stores have read
+        // it. Called before every wait of this group (a later item's loads may
+        // need the entry) and before the next staging.
+        auto kv_release = [&]() {
+            if constexpr (C::kEpiDq) {
+                if (kv_pend >= 0) {
+                    if (r == 0) {
+                        bulk_wait_read0();
+                        mbar_arrive(bar(kKvEmpty0 + kv_pend));
+                    }
+                    kv_pend = -1;
+                }
+            }
+        };
+        // One item's dK (scaled) and dV, d = 64: each thread converts its kv row
+        // (a TMEM lane) of both accumulators into the item's K/V ring entry (V
+        // entry: dV, K entry: dK; 128-byte-swizzle tiles), thread 0 stores both
+        // with TMA, and the entry is released later (kv_release). A tile ending
+        // past its sequence's slot (THD) is written row-wise from the staging.
+        // Rows past the sequence's length are zero; rows past its slot (or past
+        // s_kv, where the BSHD maps end) are not written. ks < 0: the item has no
+        // work (nothing staged; its rows in the slot get zeros).
+        auto run_epi_dq = [&](const Item& it, int ks, uint32_t acc_par) {
+            constexpr int kCpr = HD / 8;   // 16-byte chunks per row
+            kv_release();
+            bool have = ks >= 0 && ok;
+            if (have) {
+                ok = wait_group(kBarDq, 128, kAccFull, acc_par);
+                have = ok;
+                if (r == 0) SWA_TRACE(16, eacc_it);
+                if (ok) tc_fence_after();
+            }
+            const bool use_tma = !thd || it.kv_base + kTileKV <= it.s.slot_kv;
+            if (have) {
+                const bool live = it.kv_base + r < it.s.len_kv;
+#pragma unroll 1
+                for (int ts = 0; ts < 2; ++ts) {
+                    uint8_t* stg = sm + (ts == 0 ? C::kV : C::kK) + ks * C::kTile;
+                    const uint32_t col = tmem + (ts == 0 ? C::kColDV : C::kColDK) + lane_off;
+                    const float mul = ts == 0 ? 1.f : a.scale;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(col, v0);
+                    tmem_ld32(col + 32, v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float f[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            f[x] = live ? __uint_as_float(c < 4 ? v0[8 * c + x] : v1[8 * (c - 4) + x]) * mul : 0.f;
+                        *reinterpret_cast<uint4*>(stg + stg_off(r, c)) =
+                            make_uint4(pack2<BF16>(f[0], f[1]), pack2<BF16>(f[2], f[3]),
+                                       pack2<BF16>(f[4], f[5]), pack2<BF16>(f[6], f[7]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(kAccEmpty));
+                if (use_tma) fence_proxy_async_smem();
+                named_bar_sync(kBarDq, 128);
+                if (use_tma) {
+                    if (r == 0) {
+                        const int kvrow = static_cast<int>((thd ? it.s.kv_row0 : 0) + it.kv_base);
+                        tma_put(false, thd, &a.tm_dv, sbase + C::kV + ks * C::kTile, 0, static_cast<int>(it.gk),
+                                kvrow, static_cast<int>(it.bi));
+                        tma_put(false, thd, &a.tm_dk, sbase + C::kK + ks * C::kTile, 0, static_cast<int>(it.gk),
+                                kvrow, static_cast<int>(it.bi));
+                        bulk_commit();
+                        SWA_TRACE(18, eacc_it);
+                    }
+                    kv_pend = ks;
+                    return;
+                }
+            }
+            // row-wise: HD/8 threads per row, dV then dK
+            const int c = r % kCpr;
+#pragma unroll 1
+            for (int ts = 0; ts < 2; ++ts) {
+                const uint8_t* stg = sm + (ts == 0 ? C::kV : C::kK) + (ks < 0 ? 0 : ks) * C::kTile;
+                const int64_t* sst = ts == 0 ? a.dv_stride : a.dk_stride;
+                uint16_t* base = static_cast<uint16_t*>(ts == 0 ? a.dv : a.dk);
+#pragma unroll 1
+                for (int pass = 0; pass < kCpr; ++pass) {
+                    const int row = pass * (128 / kCpr) + r / kCpr;
+                    const int64_t kr = it.kv_base + row;
+                    if (kr >= it.s.slot_kv) break;   // rows ascend with the pass
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (have) w = *reinterpret_cast<const uint4*>(stg + stg_off(row, c));
+                    uint16_t* dst = base + (thd ? (it.s.kv_row0 + kr) * sst[1] : it.bi * sst[0] + kr * sst[1]) +
+                                    it.gk * sst[2] + c * 8;
+                    if (in_bounds(a.status, dst, base, ts == 0 ? g.ext.dv : g.ext.dk, 8))
+                        *reinterpret_cast<uint4*>(dst) = w;
+                }
+            }
+            if (ks >= 0) {
+                // the staging has been read: the entry goes back at once
+                named_bar_sync(kBarDq, 128);
+                if (r == 0) mbar_arrive(bar(kKvEmpty0 + ks));
+            }
+        };
         for (int64_t item = wk.begin; item < wk.end && ok; item += wk.stride) {
             const Item it = item_at(item);
-            if (!it.has_work) continue;
+            if (!it.has_work) {
+                if (C::kEpiDq && it.in_slot) run_epi_dq(it, -1, 0u);
+                continue;
+            }
+            const int eks = static_cast<int>(ekv_it % C::kKvStages);
+            const uint32_t epar = eacc_it & 1;
             for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, it.template advance<STRIP>(j, hh)) {
                 // this visit's bookkeeping first, while the dQ contraction runs
                 // (after the wait it delayed the TMEM read by ~1 K cycles)
@@ -1048,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const bool add = !STRIP && !(relay && turn == 0);
                 const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
                 const int tb = static_cast<int>(it.bi), th = static_cast<int>(hh);
+                kv_release();
                 if (r == 0) bulk_wait_read0();   // the staging is free again
                 if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
                 if (r == 0) SWA_TRACE(9, dq_it);
@@ -1382,6 +1552,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (r == 0) st_release_gpu(sem, turn + 1);
                 }
             }
+            if constexpr (C::kEpiDq) {
+                if (ok) run_epi_dq(it, eks, epar);
+            }
+            ++ekv_it;
+            ++eacc_it;
         }
         // a partner tile whose load a given-up wait did not see complete
         if (r == 0 && ld_it > 0) mbar_wait(bar(kDqLoad), (ld_it - 1) & 1, tmo);

@@ -174,6 +174,64 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Four contractions in one sequence, D (+)= A_k B_k for k = 0..3, lane 0
+// issuing: descriptor k is the first plus k * step (units of 16 bytes in the
+// start-address field, which never carries), or for an A operand in tensor
+// memory the first column plus k * step. The first contraction accumulates if
+// `accumulate` is non-zero, the other three always. One predicate setup for
+// the four, and 32-bit steps instead of 64-bit descriptor arithmetic between
+// them: the issuing warp shares its SM sub-partition with the softmax warps,
+// so its instruction count per step sets how soon the next step's
+// contractions start.
+__device__ __forceinline__ void umma_f16_ss_x4(uint32_t d_tmem, uint64_t a_desc, uint32_t a_step, uint64_t b_desc,
+                                               uint32_t b_step, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e, t;\n\t.reg .b32 l;\n\t.reg .b64 a, b, as, bs;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.u32 t, l, l;\n\t"
+        "cvt.u64.u32 as, %2;\n\t"
+        "cvt.u64.u32 bs, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
+        "add.s64 a, %1, as;\n\t"
+        "add.s64 b, %3, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+        "add.s64 a, a, as;\n\t"
+        "add.s64 b, b, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+        "add.s64 a, a, as;\n\t"
+        "add.s64 b, b, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "r"(a_step), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint32_t a_step, uint64_t b_desc,
+                                               uint32_t b_step, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e, t;\n\t.reg .b32 l, a;\n\t.reg .b64 b, bs;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.u32 t, l, l;\n\t"
+        "cvt.u64.u32 bs, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, p;\n\t"
+        "add.u32 a, %1, %2;\n\t"
+        "add.s64 b, %3, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n\t"
+        "add.u32 a, a, %2;\n\t"
+        "add.s64 b, b, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n\t"
+        "add.u32 a, a, %2;\n\t"
+        "add.s64 b, b, bs;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(a_step), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Each thread of the warp writes 8 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 {
