@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(256, 3) preprocess_kernel(const __grid_constan
             const uint32_t item = blockIdx.x + st * gridDim.x;
             if (item < n_items) issue(item, st);
         }
+    // the main kernel may start its prologue (it waits for this grid before
+    // reading anything written here)
+    grid_dep_launch();
 
     const int u = tid / TPU, half = tid % TPU;
     const int r = u / hc_n, hl = u - r * hc_n;   // this thread's unit in every block
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
     constexpr int kBatch = 4;
     const Geometry& g = a.g;
     const int tid = threadIdx.x;
+    grid_dep_wait();   // the main kernel's dQ, partials and the dSink partials
     if (a.dsink != nullptr) {
         // fixed-order finish, one CTA per head: thread t sums partials t,
         // t + 256, ... in order (eight loads in flight at a time), then a fixed
@@ -461,7 +465,22 @@ cudaError_t launch_dq_convert(const CvtArgs& a_in, int dtype, cudaStream_t s)
     // eight 256-thread CTAs fit on an SM
     const int64_t cap = int64_t(8) * sms;
     const unsigned grid = static_cast<unsigned>(units < cap ? units : cap);
-    SWA_DISPATCH(dq_convert_kernel, a, grid, s);
+    // launched with programmatic stream serialization: it waits for the main
+    // kernel in griddepcontrol.wait instead of in the launch queue
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.g.d == 64) e = dtype == 0 ? cudaLaunchKernelEx(&cfg, dq_convert_kernel<64, true>, a)
+                                    : cudaLaunchKernelEx(&cfg, dq_convert_kernel<64, false>, a);
+    else e = dtype == 0 ? cudaLaunchKernelEx(&cfg, dq_convert_kernel<128, true>, a)
+                        : cudaLaunchKernelEx(&cfg, dq_convert_kernel<128, false>, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -174,6 +174,15 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Programmatic dependent launch. launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) start its
+// prologue before this one ends; wait, in that next kernel, blocks until the
+// previous kernel has completed and its memory is visible. Without the launch
+// attribute both are no-ops in effect: the kernel starts after its
+// predecessor anyway.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Four contractions in one sequence, D (+)= A_k B_k for k = 0..3, lane 0
 // issuing: descriptor k is the first plus k * step (units of 16 bytes in the
 // start-address field, which never carries), or for an A operand in tensor
