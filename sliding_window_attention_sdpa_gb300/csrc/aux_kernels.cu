@@ -382,13 +382,25 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const CvtArgs a)
                 const float* src = a.dq_part +
                                    (((bi * g.h_q + h0 + hl) * a.n_q_tiles + j) * a.n_slots * kTileQ + r) * HD + c * 8;
                 float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // eight visitors' loads in flight, then their sums in visitor order
 #pragma unroll 1
-                for (int64_t v = 0; v < nv; ++v) {
-                    if (!in_bounds(a.status, src + v * kTileQ * HD, a.dq_part, g.ext.dq_part, 8)) continue;
-                    const float4 xv = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[0];
-                    const float4 yv = reinterpret_cast<const float4*>(src + v * kTileQ * HD)[1];
-                    f[0] += xv.x; f[1] += xv.y; f[2] += xv.z; f[3] += xv.w;
-                    f[4] += yv.x; f[5] += yv.y; f[6] += yv.z; f[7] += yv.w;
+                for (int64_t v0 = 0; v0 < nv; v0 += 8) {
+                    float4 xv[8], yv[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        xv[q] = yv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float* pv = src + (v0 + q) * kTileQ * HD;
+                        if (v0 + q < nv && in_bounds(a.status, pv, a.dq_part, g.ext.dq_part, 8)) {
+                            xv[q] = reinterpret_cast<const float4*>(pv)[0];
+                            yv[q] = reinterpret_cast<const float4*>(pv)[1];
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (v0 + q >= nv) break;
+                        f[0] += xv[q].x; f[1] += xv[q].y; f[2] += xv[q].z; f[3] += xv[q].w;
+                        f[4] += yv[q].x; f[5] += yv[q].y; f[6] += yv[q].z; f[7] += yv[q].w;
+                    }
                 }
                 uint16_t* dst = dst_of(t0 + r, h0 + hl, c);
                 if (in_bounds(a.status, dst, a.dq, g.ext.dq, 8))
