@@ -355,23 +355,30 @@ struct ItemCounts {
 //    partitions. The previous kv-tile of the same head (the dQ relay partner)
 //    is item - h_kv, which runs in the same wave.
 //  - Strip mode: items numbered (kv-head, sequence, kv-tile), kv-tile
-//    fastest; the grid is R CTAs per kv-head and CTA c walks kv-head c % h_kv
-//    over the (c / h_kv)-th of R equal contiguous runs of that head's
-//    (sequence, kv-tile) items, so that the two kv-tiles visiting a q-tile are
-//    consecutive items of one CTA except where a run ends. The CTAs on one run
-//    index read the same token rows of every head at about the same time, as
-//    the round-robin walk does.
+//    fastest. Groups of G consecutive kv-heads (G chosen by the launcher so
+//    that the grid fills the SMs: 16 kv-heads on 152 SMs take G = 2, 19 runs
+//    per group) share R equal contiguous runs of their items; CTA c walks
+//    group c % (h_kv / G) over run c / (h_kv / G). The two kv-tiles visiting
+//    a q-tile are then consecutive items of one CTA except where a run ends.
+//    A run may cross from one kv-head or sequence into the next: no q-tile
+//    has visitors on both sides of such a boundary (a sequence's first
+//    kv-tile is the first visitor of each of its q-tiles), so no pair is
+//    formed across it. The CTAs on one run index read the same token rows of
+//    every group at about the same time, as the round-robin walk does.
 struct Walk {
     int64_t begin, end, stride;
 };
 
 template <bool STRIP>
-__device__ __forceinline__ Walk item_walk(int64_t n_items, int64_t h_kv)
+__device__ __forceinline__ Walk item_walk(int64_t n_items, int64_t h_kv, int64_t group_heads)
 {
     if constexpr (STRIP) {
-        const int64_t runs = gridDim.x / h_kv, g = blockIdx.x % h_kv, run = blockIdx.x / h_kv;
-        const int64_t per_head = n_items / h_kv;
-        return Walk{g * per_head + per_head * run / runs, g * per_head + per_head * (run + 1) / runs, 1};
+        // groups of group_heads consecutive kv-heads share R runs: CTA c walks
+        // group c % (h_kv / group_heads) over the (c / ...)-th run of its items
+        const int64_t n_groups = h_kv / group_heads;
+        const int64_t runs = gridDim.x / n_groups, grp = blockIdx.x % n_groups, run = blockIdx.x / n_groups;
+        const int64_t per_group = n_items / h_kv * group_heads;
+        return Walk{grp * per_group + per_group * run / runs, grp * per_group + per_group * (run + 1) / runs, 1};
     }
     return Walk{static_cast<int64_t>(blockIdx.x), n_items, static_cast<int64_t>(gridDim.x)};
 }
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const bool thd = g.layout == 1;
     const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
                          static_cast<uint32_t>(g.h_q / g.h_kv), static_cast<uint32_t>(g.b)};
-    const Walk wk = item_walk<STRIP>(n_items, g.h_kv);
+    const Walk wk = item_walk<STRIP>(n_items, g.h_kv, a.strip > 0 ? a.strip : 1);
 
     if (tid == 0) {
         misc[1] = 0;
@@ -1591,15 +1598,27 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     int64_t grid = items < sms ? items : sms;
+    int64_t group_heads = 1;
     if constexpr (STRIP) {
-        // R runs per kv-head, at least one item each (the host falls back to
-        // the round-robin walk when there are more kv-heads than SMs)
+        // R runs per group of G kv-heads, at least one item each. The
+        // smallest G that fills the most SMs (G = 1 for the lockstep of every
+        // head; the host falls back to the round-robin walk when there are
+        // more kv-heads than SMs).
         const int64_t per_head = items / a.g.h_kv;
-        int64_t runs = sms / a.g.h_kv;
-        if (runs > per_head) runs = per_head;
-        grid = runs * a.g.h_kv;
+        int64_t best = 0;
+        for (int64_t G = 1; G <= a.g.h_kv && G <= 8; G *= 2) {
+            if (a.g.h_kv % G) continue;
+            int64_t runs = sms * G / a.g.h_kv;
+            if (runs > per_head * G) runs = per_head * G;
+            if (runs * (a.g.h_kv / G) > best) {
+                best = runs * (a.g.h_kv / G);
+                group_heads = G;
+            }
+        }
+        grid = best;
     }
     MainArgs b = a;
+    if constexpr (STRIP) b.strip = static_cast<int32_t>(group_heads);
     b.use_items = items <= kItemTableMaxPerCta * grid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -145,11 +145,12 @@ struct MainArgs {
     // items; with many, the roles decode in place)
     void* items;
     int32_t use_items;
-    // Strip mode (the launcher sets it when no q-tile can have more than two
-    // visiting kv-tiles, d = 64): each CTA walks a contiguous run of work items
+    // Strip mode (non-zero when no q-tile can have more than two visiting
+    // kv-tiles, d = 64): each CTA walks a contiguous run of work items
     // numbered kv-tile fastest and sweeps each item's q-tiles from the bottom
     // up, so that the two visitors of a q-tile are consecutive steps of one CTA
-    // except where the run ends.
+    // except where the run ends. The main kernel's launcher sets it to the
+    // number of consecutive kv-heads whose items share one set of runs.
     int32_t strip;
     // Test hook (zero in normal use): bit 0 makes every relay turn wait for a
     // counter value no visitor writes, bit 1 makes the second arrival of a
