@@ -72,6 +72,11 @@ SMALL = [
          thd_lens=[390, 64, 1000, 129], slot_align=8, seed=26),
     Case("thd_strip_mha_40seq_w128_rowwise_det", 0, 1, 1, 0, 0, 64, "tl", 128, layout="thd",
          thd_lens=[300 + (37 * i) % 300 for i in range(40)], slot_align=8, det=True, seed=27),
+    # strip mode with 16 kv-heads: pairs of kv-heads share 19 runs, so runs
+    # cross from one kv-head's items into the next (MHA pairs in tensor
+    # memory, and GQA pairs through the accumulator rows)
+    Case("strip_headpair_b1_h16_s2560_w128_det", 1, 16, 16, 2560, 2560, 64, "tl", 128, det=True, seed=28),
+    Case("strip_headpair_gqa32x16_s1280_w128", 1, 32, 16, 1280, 1280, 64, "tl", 128, seed=29),
 ]
 
 
