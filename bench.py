@@ -266,7 +266,7 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "7748a57631958ecf", "bytes": 282760192},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "46ca7e380ee727be", "bytes": 283659008},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).

@@ -574,7 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         return bar_and(id, count, wait(b, parity));
     };
 
+    // Register split at d = 64 (the launch gives each thread 128 registers, the
+    // whole register file). With 128 each the dQ role spilled, and the dQ warps
+    // (dQ, and each item's dK/dV epilogue) pace the MMA warp through DqEmpty
+    // and AccEmpty. The producer, MMA and idle warps give 16 each to the dQ
+    // warps: x + 128 + 128 + y = 512 per lane of the four warpgroups, x = 112,
+    // y = 144. Main kernel: headline 93 -> 90 us, W512 621 -> 592 us,
+    // non-square W8000 506 -> 474 us. At d = 128 the same split made the
+    // b12 h48/6 S16484 case 5% slower, so that kernel keeps 128 everywhere.
     if (warp == kWarpTma) {
+        if constexpr (C::kAhead) asm volatile("setmaxnreg.dec.sync.aligned.u32 112;");
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, q_it = 0;
@@ -629,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 mbar_wait(bar(kQFull0 + i % C::kStages), (i / C::kStages) & 1, tmo);
         }
     } else if (warp == kWarpMma) {
+        if constexpr (C::kAhead) asm volatile("setmaxnreg.dec.sync.aligned.u32 112;");
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
         constexpr uint32_t kIdPV = idesc_f16(BF16, 128, HD, false, true);
@@ -813,6 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         umma_commit(bar(kDrain));
         mbar_wait(bar(kDrain), 0, tmo);
     } else if (warp < kWarpSoft0) {
+        if constexpr (C::kAhead) asm volatile("setmaxnreg.dec.sync.aligned.u32 112;");
         // warps 2-3: no role
     } else if (warp < kWarpDq0) {
         // ------------------------------------------------------------ softmax + dK/dV epilogue
@@ -1055,6 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         }
         if constexpr (C::kPInTmem) tmem_st_wait();   // a step left early may have P^T stores in flight
     } else {
+        if constexpr (C::kAhead) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;");
         // ------------------------------------------------------------ dQ
         // Visitors of a q-tile are the contiguous kv-tiles [first, first + n).
         //  - n == 1: the lone visitor converts its dQ rows and stores them.
