@@ -684,27 +684,20 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     umma_f16_ts_x4(tm_dv, tmem + C::kColP, 8, dDOmn, 2048 >> 4, kIdPV, acc);
                     umma_f16_ts_x4(tm_dv, tmem + C::kColP + 32, 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
                 } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dv, sdesc_sw128(sbase + C::kP + aoff, 16, 1024), sdesc_at(dDOmn, k * 2048),
-                                    kIdPV, acc | (k > 0));
-                    }
+                    // P^T in shared memory: columns 16 k (32 bytes, then the next 16 KB block)
+                    const uint64_t dP0 = sdesc_sw128(sbase + C::kP, 16, 1024);
+                    umma_f16_ss_x4(tm_dv, dP0, 32 >> 4, dDOmn, 2048 >> 4, kIdPV, acc);
+                    umma_f16_ss_x4(tm_dv, sdesc_at(dP0, kBlock16K), 32 >> 4, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4,
+                                   kIdPV, 1);
                 }
                 // P^T is free (and, with everything issued before, the dS^T
                 // buffer of the step before this one)
                 if constexpr (C::kAhead) umma_commit(bar(kPEmpty));
-                if constexpr (C::kAhead) {
+                {
                     // dS^T columns 16 k (32 bytes, then the next 16 KB block), Q rows 16 k
                     umma_f16_ss_x4(tm_dk, dDSk, 32 >> 4, dQmn, 2048 >> 4, kIdPV, acc);
                     umma_f16_ss_x4(tm_dk, sdesc_at(dDSk, kBlock16K), 32 >> 4, sdesc_at(dQmn, 4 * 2048), 2048 >> 4,
                                    kIdPV, 1);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t aoff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                        umma_f16_ss(tm_dk, sdesc_at(dDSk, aoff), sdesc_at(dQmn, k * 2048), kIdPV, acc | (k > 0));
-                    }
                 }
                 // Q and dO have been read (dQ below reads only dS and K): the
                 // stage goes back to the producer
@@ -722,16 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             {
                 tc_fence_after();
                 const uint64_t dKmn = sdesc_at(dKmn0, kv_off), dDSmn = sdesc_at(dDSmn0, ds_off);
-                if constexpr (C::kAhead) {
+                {
                     // dS rows and K rows 16 k (2 KB each)
                     umma_f16_ss_x4(tm_dq, dDSmn, 2048 >> 4, dKmn, 2048 >> 4, kIdDQ, dq_onto);
                     umma_f16_ss_x4(tm_dq, sdesc_at(dDSmn, 4 * 2048), 2048 >> 4, sdesc_at(dKmn, 4 * 2048), 2048 >> 4,
                                    kIdDQ, 1);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        umma_f16_ss(tm_dq, sdesc_at(dDSmn, k * 2048), sdesc_at(dKmn, k * 2048), kIdDQ,
-                                    k > 0 || dq_onto);
                 }
                 if (p.tpair != 1) umma_commit(bar(kDqFull));
                 SWA_TRACE(4, p.q_it);
@@ -782,22 +770,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (C::kDqAliasesS && !(ok = wait_warp(kDqEmpty, (dq_it & 1) ^ 1))) break;
                 {
                     tc_fence_after();
-                    if constexpr (HD == 64) {
-                        // contraction step k: 32 bytes into the rows of K, Q, V, dO
-                        umma_f16_ss_x4(tm_s, dK, 32 >> 4, dQ, 32 >> 4, kIdQK, 0);
-                        umma_f16_ss_x4(tm_dp, dV, 32 >> 4, dDO, 32 >> 4, kIdQK, 0);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < HD / 16; ++k) {
-                            const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                            umma_f16_ss(tm_s, sdesc_at(dK, koff), sdesc_at(dQ, koff), kIdQK, k > 0);
-                        }
-#pragma unroll
-                        for (int k = 0; k < HD / 16; ++k) {
-                            const uint32_t koff = (k >> 2) * kBlock16K + (k & 3) * 32;
-                            umma_f16_ss(tm_dp, sdesc_at(dV, koff), sdesc_at(dDO, koff), kIdQK, k > 0);
-                        }
-                    }
+                    // contraction step k: 32 bytes into the rows of K, Q, V, dO (then,
+                    // at d = 128, the same in the second 64-column block)
+                    umma_f16_ss_x4(tm_s, dK, 32 >> 4, dQ, 32 >> 4, kIdQK, 0);
+                    if constexpr (HD == 128)
+                        umma_f16_ss_x4(tm_s, sdesc_at(dK, kBlock16K), 32 >> 4, sdesc_at(dQ, kBlock16K), 32 >> 4,
+                                       kIdQK, 1);
+                    umma_f16_ss_x4(tm_dp, dV, 32 >> 4, dDO, 32 >> 4, kIdQK, 0);
+                    if constexpr (HD == 128)
+                        umma_f16_ss_x4(tm_dp, sdesc_at(dV, kBlock16K), 32 >> 4, sdesc_at(dDO, kBlock16K), 32 >> 4,
+                                       kIdQK, 1);
                     umma_commit(bar(kSFull));
                     SWA_TRACE(1, q_it);
                 }
