@@ -141,10 +141,10 @@ int64_t max_visitors(const sdpa_bwd_params* p)
     return v < nkv ? v : nkv;
 }
 
-// Strip mode of the main kernel (d = 64, at most two visitors per q-tile): the
-// two visitors of a q-tile combine dQ inside one CTA, or by arrival order
-// between two, without the relay or per-visitor slots.
-bool strip_mode(const sdpa_bwd_params* p) { return p->d == 64 && max_visitors(p) <= 2; }
+// Strip mode of the main kernel (at most two visitors per q-tile): the two
+// visitors of a q-tile combine dQ inside one CTA, or by arrival order between
+// two, without the relay or per-visitor slots.
+bool strip_mode(const sdpa_bwd_params* p) { return max_visitors(p) <= 2; }
 
 // Most workspace the per-visitor dQ slots may take; beyond it deterministic
 // mode keeps the relay.

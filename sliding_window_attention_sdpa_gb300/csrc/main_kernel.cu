@@ -117,7 +117,9 @@ struct Cfg {
 // mbarrier indices
 enum Bar : int {
     kSFull = 0, kPFull, kPEmpty, kDqFull, kDqEmpty, kAccFull, kAccEmpty,
-    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kDqLoad, kDrain, kNumBars
+    kQFull0, kQFull1, kQEmpty0, kQEmpty1, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kDqLoad, kDrain,
+    kDqLoad1,   // d = 128: the second half of a stored dQ partial (kDqLoad: the first)
+    kNumBars
 };
 
 template <bool BF16>
@@ -219,6 +221,22 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, ui
 {
     if (thd) tma_load_3d(dst, map, bar, c0, head, row);
     else tma_load_4d(dst, map, bar, c0, head, row, batch);
+}
+
+// Starts moving one box of a tensor map (coordinates as for tma_box) into L2.
+// Nothing completes or is waited for: later loads of those rows find them in L2.
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, bool thd, int c0, int head, int row, int batch)
+{
+    if (thd)
+        asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                         reinterpret_cast<uint64_t>(map)),
+                     "r"(c0), "r"(head), "r"(row)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                         reinterpret_cast<uint64_t>(map)),
+                     "r"(c0), "r"(head), "r"(row), "r"(batch)
+                     : "memory");
 }
 
 // Loads rows [row, row + 128) of one head of a [., HD] tensor into a swizzled tile
@@ -520,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         mbar_init(bar(kAccFull), 1);
         mbar_init(bar(kAccEmpty), C::kEpiDq ? 128 : kSoftThreads);
         mbar_init(bar(kDqLoad), 1);
+        mbar_init(bar(kDqLoad1), 1);
         mbar_init(bar(kDrain), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(kQFull0 + s), 1);
@@ -541,10 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     // slower.
     Item* items = static_cast<Item*>(a.items);
     const bool use_items = C::kAhead && a.use_items != 0;
+    // Strip mode pairs a q-tile's two dQ contractions in tensor memory only
+    // where dQ has columns of its own (d = 64); at d = 128 it aliases S^T,
+    // which the next step overwrites, so the pair goes through the
+    // accumulator rows instead.
+    constexpr bool kTmemPairs = STRIP && !C::kDqAliasesS;
     if (use_items)
         for (int64_t item = wk.begin + static_cast<int64_t>(tid) * wk.stride; item < wk.end;
              item += static_cast<int64_t>(kThreads) * wk.stride)
-            items[item] = with_pairs<STRIP>(g, decode<STRIP>(a, cnt, item), item, wk);
+            items[item] = with_pairs<kTmemPairs>(g, decode<STRIP>(a, cnt, item), item, wk);
     auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode<STRIP>(a, cnt, i); };
     tc_fence_before();
     __syncthreads();   // also publishes the item table to the CTA
@@ -737,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         };
         bool ok = true;
         for (int64_t item = wk.begin; item < wk.end && ok; item += wk.stride) {
-            const Item it = use_items ? items[item] : with_pairs<STRIP>(g, item_at(item), item, wk);
+            const Item it = use_items ? items[item] : with_pairs<kTmemPairs>(g, item_at(item), item, wk);
             if (!it.has_work) continue;
             const int ks = kv_it % C::kKvStages;
             if (!(ok = wait_warp(kKvFull0 + ks, (kv_it / C::kKvStages) & 1))) break;
@@ -755,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 }
                 // this step's bookkeeping and operand descriptors, ahead of the
                 // wait for the softmax
-                const int tp = it.steps <= 2 ? (k == 0 ? it.tp_first : it.tp_last) : tmem_pair<STRIP>(g, it, j, item, wk);
+                const int tp = it.steps <= 2 ? (k == 0 ? it.tp_first : it.tp_last) : tmem_pair<kTmemPairs>(g, it, j, item, wk);
                 const Pending cur{true, k == 0, k + 1 == it.steps, st, ks, q_it, tp};
                 const uint64_t dK = sdesc_at(dK0, ks * C::kTile), dQ = sdesc_at(dQ0, st * C::kTile);
                 const uint64_t dV = sdesc_at(dV0, ks * C::kTile), dDO = sdesc_at(dDO0, st * C::kTile);
@@ -1068,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint8_t* stg = sm + C::kDqStage;
         const uint32_t stg_s = sbase + C::kDqStage;
-        uint32_t dq_it = 0, ld_it = 0;
+        uint32_t dq_it = 0, ld_it = 0, ld1_it = 0;
         bool ok = true;
         // d = 64 dK/dV epilogue state: K/V ring entry an issued store may still
         // be reading (-1: none), and the counters of items with work (their
@@ -1206,7 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const bool local = STRIP && nvis == 2 && (turn == 0 ? item + 1 < wk.end : item > wk.begin);
                 // one q-head per kv-head: the pair's dQ adds up in tensor memory
                 // (tmem_pair); the first step reads nothing, the second the sum
-                const int tpair = local && it.group == 1 ? 1 + turn : 0;
+                const int tpair = kTmemPairs && local && it.group == 1 ? 1 + turn : 0;
                 if (tpair == 1) continue;
                 const bool pair = STRIP && nvis == 2 && !local;
                 const bool single = nvis <= 1 || tpair == 2;   // no partial to combine
@@ -1226,7 +1250,52 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const int qrow = static_cast<int>((thd ? it.s.q_row0 : 0) + j * kTileQ);
                 const int tb = static_cast<int>(it.bi), th = static_cast<int>(hh);
                 kv_release();
+                if (STRIP && C::kDqAliasesS && r == 0) {
+                    // Strip mode at d = 128: the second visitor of a pair inside this
+                    // CTA's run reads the partial that the first stored one item
+                    // earlier, by then often out of L2, while its dQ columns (and so
+                    // the next S^T) wait. Move it back for the next step (of this
+                    // item, or the next item's first) while this one runs.
+                    int64_t j2 = j, h2 = hh;
+                    Item nx = it;
+                    bool have = true;
+                    if (k + 1 < it.steps) {
+                        it.template advance<STRIP>(j2, h2);
+                    } else if (item + wk.stride < wk.end) {
+                        nx = item_at(item + wk.stride);
+                        j2 = nx.first_j<STRIP>();
+                        h2 = nx.h0;
+                        have = nx.has_work;
+                    } else {
+                        have = false;
+                    }
+                    if (have) {
+                        int64_t f2, n2;
+                        q_tile_visitors(g, nx.s, j2, f2, n2);
+                        if (n2 == 2 && nx.t - f2 == 1 && (!thd || (j2 + 1) * kTileQ <= nx.s.slot_q)) {
+                            const int row2 = static_cast<int>((thd ? nx.s.q_row0 : 0) + j2 * kTileQ);
+#pragma unroll
+                            for (int c = 0; c < HD; c += 32)
+                                tma_prefetch_l2(&a.tm_acc, thd, c, static_cast<int>(h2), row2, static_cast<int>(nx.bi));
+                        }
+                    }
+                }
                 if (r == 0) bulk_wait_read0();   // the staging is free again
+                // d = 128, second step of a pair inside this CTA's run: the partial
+                // was stored an item ago, so its first half comes into the staging
+                // while the dQ contraction runs
+                const bool pre0 = C::kDqAliasesS && lpair && turn == 1 && use_tma && k + 1 < it.steps;
+                const uint32_t pre_ld = ld_it;
+                if (pre0) {
+                    if (r == 0) {
+                        bulk_wait0();   // this thread stored the partial
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
+                        tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
+                        tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
+                    }
+                    ++ld_it;
+                }
                 if (!(ok = wait_group(kBarDq, 128, kDqFull, dq_it & 1))) break;
                 if (r == 0) SWA_TRACE(9, dq_it);
                 ++dq_it;
@@ -1471,7 +1540,75 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     // With a partial sum to add, the row-wise path loads it eight
                     // rows at a time; read per row here, its latency would hold
                     // the dQ columns of TMEM (aliasing S^T) four times over.
-                    if (conv_now && use_tma && single) {
+                    if (conv_now && use_tma && go && !single && k + 1 < it.steps) {
+                        // Adds the stored partial and converts, a 64-column half at a
+                        // time: the fp32 partial comes by TMA (half 0 into the staging,
+                        // half 1 into the P^T buffer, idle from the dQ contraction to
+                        // this group's release; an item's last step leaves it to the
+                        // dK/dV epilogue), this visit's dQ from TMEM, and each half of
+                        // the 16-bit tile goes out from the staging.
+                        uint32_t ld0 = pre_ld;
+                        if (!pre0) {
+                            ld0 = ld_it++;
+                            if (r == 0) {
+                                if (lpair) {
+                                    bulk_wait0();   // this thread stored the partial
+                                    fence_proxy_async_global();
+                                }
+                                mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
+                                tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
+                                tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
+                            }
+                        }
+                        const uint32_t ld1 = ld1_it++;
+                        if (r == 0) {
+                            mbar_arrive_expect_tx(bar(kDqLoad1), 2 * kBlock16K);
+                            tma_box(sbase + C::kP, &a.tm_acc, bar(kDqLoad1), thd, 64, th, qrow, tb);
+                            tma_box(sbase + C::kP + kBlock16K, &a.tm_acc, bar(kDqLoad1), thd, 96, th, qrow, tb);
+                        }
+#pragma unroll 1
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t v0[32], v1[32];
+                            tmem_ld32(tmem + C::kColDQ + lane_off + 64 * hf, v0);
+                            tmem_ld32(tmem + C::kColDQ + lane_off + 64 * hf + 32, v1);
+                            tmem_ld_wait();
+                            const bool got = hf == 0 ? wait_group(kBarDq, 128, kDqLoad, ld0 & 1)
+                                                     : wait_group(kBarDq, 128, kDqLoad1, ld1 & 1);
+                            const uint8_t* src = hf == 0 ? stg : sm + C::kP;
+                            if (got) {
+                                // 16-bit chunk i of the half (columns 8i..8i+7) from fp32
+                                // chunks 2i, 2i+1; written to staging chunk 8 hf + i
+                                // (half 0 in place, over fp32 chunks already read)
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float4 x0 = *reinterpret_cast<const float4*>(src + stg_off(r, 2 * i));
+                                    const float4 x1 = *reinterpret_cast<const float4*>(src + stg_off(r, 2 * i + 1));
+                                    const uint32_t* v = i < 4 ? v0 + 8 * i : v1 + 8 * (i - 4);
+                                    // strip mode: own partial rounded, then one add (a
+                                    // two-term sum that does not depend on which came
+                                    // first); the relay adds in turn order
+                                    auto sum = [&](int e, float x) {
+                                        return STRIP ? __fadd_rn(__fmul_rn(__uint_as_float(v[e]), a.scale), x)
+                                                     : fmaf(__uint_as_float(v[e]), a.scale, x);
+                                    };
+                                    *reinterpret_cast<uint4*>(stg + stg_off(r, 8 * hf + i)) = make_uint4(
+                                        pack2<BF16>(sum(0, x0.x), sum(1, x0.y)), pack2<BF16>(sum(2, x0.z), sum(3, x0.w)),
+                                        pack2<BF16>(sum(4, x1.x), sum(5, x1.y)), pack2<BF16>(sum(6, x1.z), sum(7, x1.w)));
+                                }
+                            }
+                            if (hf == 1) {
+                                // TMEM and the P^T buffer have been read
+                                tc_fence_before();
+                                mbar_arrive(bar(kDqEmpty));
+                            }
+                            fence_proxy_async_smem();
+                            named_bar_sync(kBarDq, 128);
+                            if (r == 0 && got) {
+                                tma_put(false, thd, &a.tm_dq, stg_s + hf * kBlock16K, 64 * hf, th, qrow, tb);
+                                bulk_commit();
+                            }
+                        }
+                    } else if (conv_now && use_tma && single) {
 #pragma unroll 1
                         for (int ch = 0; ch < HD / 32; ++ch) {
                             uint32_t v[32];
@@ -1518,6 +1655,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                     bulk_commit();
                                 }
                             } else if (go) {
+                                if (lpair && rd == 0 && r == 0) {
+                                    // this thread stored the partial in an earlier step
+                                    bulk_wait0();
+                                    fence_proxy_async_global();
+                                }
                                 apply(rd * 64);
                             } else {
                                 named_bar_sync(kBarDq, 128);
@@ -1568,6 +1710,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
         }
         // a partner tile whose load a given-up wait did not see complete
         if (r == 0 && ld_it > 0) mbar_wait(bar(kDqLoad), (ld_it - 1) & 1, tmo);
+        if (r == 0 && ld1_it > 0) mbar_wait(bar(kDqLoad1), (ld1_it - 1) & 1, tmo);
     }
 
     bulk_wait0();   // copies issued from this CTA's shared memory are complete
@@ -1639,6 +1782,7 @@ cudaError_t launch_main(const MainArgs& a, int dtype, cudaStream_t s)
         if (a.strip) return dtype == 0 ? launch_typed<64, true, true>(a, s) : launch_typed<64, false, true>(a, s);
         return dtype == 0 ? launch_typed<64, true, false>(a, s) : launch_typed<64, false, false>(a, s);
     }
+    if (a.strip) return dtype == 0 ? launch_typed<128, true, true>(a, s) : launch_typed<128, false, true>(a, s);
     return dtype == 0 ? launch_typed<128, true, false>(a, s) : launch_typed<128, false, false>(a, s);
 }
 

@@ -77,6 +77,15 @@ SMALL = [
     # memory, and GQA pairs through the accumulator rows)
     Case("strip_headpair_b1_h16_s2560_w128_det", 1, 16, 16, 2560, 2560, 64, "tl", 128, det=True, seed=28),
     Case("strip_headpair_gqa32x16_s1280_w128", 1, 32, 16, 1280, 1280, 64, "tl", 128, seed=29),
+    # strip mode at d = 128, where dQ shares its tensor-memory columns with
+    # S^T: every pair goes through the accumulator rows (one head per kv-head,
+    # deterministic; THD tiles that end past their slot, and 40 one-head
+    # sequences whose pairs are split between CTAs)
+    Case("strip_d128_mha_b2_h4_s1300_w128_det", 2, 4, 4, 1300, 1300, 128, "tl", 128, det=True, seed=30),
+    Case("thd_strip_d128_gqa4x2_w100_rowwise", 0, 4, 2, 0, 0, 128, "tl", 100, layout="thd",
+         thd_lens=[390, 64, 1000, 129], slot_align=8, seed=31),
+    Case("thd_strip_d128_mha_40seq_w128_rowwise_det", 0, 1, 1, 0, 0, 128, "tl", 128, layout="thd",
+         thd_lens=[300 + (37 * i) % 300 for i in range(40)], slot_align=8, det=True, seed=32),
 ]
 
 
