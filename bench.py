@@ -53,6 +53,9 @@ WORKLOADS = {
     "gptoss_b2_h16_d64_w128_s32768": (2, 16, 16, 32768, 32768, 64, "tl", 128, "bf16"),
     "gqa_b12_h48x6_d128_s16484_br_w96": (12, 48, 6, 16484, 16484, 128, "br", 96, "bf16"),
     "gqa_b24_h28x4_d128_s128_br_w8000": (24, 28, 4, 128, 128, 128, "br", 8000, "f16"),
+    # one sequence of the shape above: small enough for a full ncu capture of
+    # the d = 128 main kernel (~1.3 GB on the device)
+    "gqa_b1_h48x6_d128_s16484_br_w96": (1, 48, 6, 16484, 16484, 128, "br", 96, "bf16"),
     "nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000": (12, 40, 8, 128, 8960, 64, "br", 8000, "bf16"),
     "winonly_b4_h16_d64_s4096_w512": (4, 16, 16, 4096, 4096, 64, "none", 512, "bf16"),
 }
@@ -266,12 +269,12 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "46ca7e380ee727be", "bytes": 283659008},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "f893b1cdc1c763f7", "bytes": 282436864},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
 FWD_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "fe72f0d94bac4b1d", "bytes": 114089216},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "1a167d12b75e8039", "bytes": 114572544},
 }
 FWD_SOURCES = ("fwd_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 
