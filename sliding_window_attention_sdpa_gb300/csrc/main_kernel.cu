@@ -1281,10 +1281,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     }
                 }
                 if (r == 0) bulk_wait_read0();   // the staging is free again
-                // d = 128, second step of a pair inside this CTA's run: the partial
-                // was stored an item ago, so its first half comes into the staging
-                // while the dQ contraction runs
-                const bool pre0 = C::kDqAliasesS && lpair && turn == 1 && use_tma && k + 1 < it.steps;
+                // Second step of a pair inside this CTA's run: the partial was stored
+                // an item ago, so it (at d = 128 its first half) comes into the
+                // staging while the dQ contraction runs
+                const bool pre0 = lpair && turn == 1 && use_tma && (!C::kDqAliasesS || k + 1 < it.steps);
                 const uint32_t pre_ld = ld_it;
                 if (pre0) {
                     if (r == 0) {
@@ -1467,20 +1467,19 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (go) {
                         if (conv_now && use_tma && !single) {
                             // the earlier visitors' partial sum: one TMA load of the
-                            // fp32 tile into the staging; each thread then adds its
-                            // row and writes it back converted, in place
-                            if (r == 0) {
-                                if (lpair) {
-                                    // this thread stored the partial in an earlier step
-                                    bulk_wait0();
-                                    fence_proxy_async_global();
+                            // fp32 tile into the staging (issued above for a pair
+                            // inside the run); each thread then adds its row and
+                            // writes it back converted, in place
+                            uint32_t ldi = pre_ld;
+                            if (!pre0) {
+                                ldi = ld_it++;
+                                if (r == 0) {
+                                    mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
+                                    tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
+                                    tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
                                 }
-                                mbar_arrive_expect_tx(bar(kDqLoad), 2 * kBlock16K);
-                                tma_box(stg_s, &a.tm_acc, bar(kDqLoad), thd, 0, th, qrow, tb);
-                                tma_box(stg_s + kBlock16K, &a.tm_acc, bar(kDqLoad), thd, 32, th, qrow, tb);
                             }
-                            const bool got = wait_group(kBarDq, 128, kDqLoad, ld_it & 1);
-                            ++ld_it;
+                            const bool got = wait_group(kBarDq, 128, kDqLoad, ldi & 1);
                             if (got) {
                                 // 16-bit chunk i (columns 8i..8i+7) from fp32 chunks 2i,
                                 // 2i+1; it lands where fp32 chunk i was, already used
