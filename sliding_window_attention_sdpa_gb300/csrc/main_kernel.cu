@@ -83,9 +83,11 @@ struct Cfg {
     static constexpr uint32_t kV = kK + kKvStages * kTile;      // kKvStages tiles
     static constexpr uint32_t kQ = kV + kKvStages * kTile;      // kStages tiles
     static constexpr uint32_t kDO = kQ + kStages * kTile;       // kStages tiles
-    static constexpr bool kPInTmem = HD == 64;                  // P^T kept in TMEM
-    static constexpr uint32_t kP = kDO + kStages * kTile;       // P^T  [128 kv x 128 q] (d = 128)
-    static constexpr uint32_t kDS = kP + (kPInTmem ? 0 : 32768); // kDsBufs x dS^T [128 kv x 128 q]
+    // P^T is kept in TMEM (the A operand of dV); at d = 128 a 32 KB region at kP
+    // stays for the dK/dV epilogue's staging
+    static constexpr bool kPInTmem = true;
+    static constexpr uint32_t kP = kDO + kStages * kTile;       // epilogue staging (d = 128)
+    static constexpr uint32_t kDS = kP + (HD == 64 ? 0 : 32768); // kDsBufs x dS^T [128 kv x 128 q]
     // dQ staging: 128 rows x 64 fp32 (two 16 KB blocks of 32 columns; the whole
     // row at d = 64, half of it at d = 128), or the whole 16-bit dQ tile
     static constexpr int kDqCols = 64;
@@ -98,12 +100,21 @@ struct Cfg {
     // The dK/dV epilogue stages two 128 x HD 16-bit tiles (2 x 16 KB at d = 64,
     // 2 x 32 KB at d = 128) in a dS^T buffer (d = 64) or in the P^T + dS^T
     // buffers (d = 128), all idle once the work item's contractions are done.
-    static_assert(kPInTmem ? 2 * 128 * HD * 2 <= 32768 : (kDS == kP + 32768 && 2 * 128 * HD * 2 <= 65536),
+    static_assert(HD == 64 ? 2 * 128 * HD * 2 <= 32768 : (kDS == kP + 32768 && 2 * 128 * HD * 2 <= 65536),
                   "epilogue staging does not fit");
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
     static constexpr uint32_t kColDQ = HD == 64 ? 384 : 0;
-    static constexpr uint32_t kColP = 448;                      // d = 64 only
+    // P^T's TMEM column for 16-bit chunk sc (q columns 16 sc .. 16 sc + 15, two
+    // to a column): at d = 64 its own columns 448-511; at d = 128 over the dP^T
+    // columns already read by the warp that writes it (the half of the q-tile
+    // at column 64 h goes to dP^T's columns 128 + 64 h ..., which hold its
+    // chunks 4 h, 4 h + 1 and are read before chunk 4 h + 2 is written)
+    static constexpr uint32_t kColP = 448;
+    static __host__ __device__ constexpr uint32_t p_col(int sc)
+    {
+        return HD == 64 ? kColP + 8u * sc : 128u + 64u * (sc >> 2) + 8u * (sc & 3);
+    }
     static constexpr bool kDqAliasesS = HD != 64;
     // d = 64: the dQ warps write each item's dK/dV, staged in the item's own
     // K/V ring entry (idle once its last contractions are done), and hand the
@@ -704,9 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const uint64_t dDOmn = sdesc_at(dDOmn0, q_off), dQmn = sdesc_at(dQmn0, q_off);
                 const uint64_t dDSk = sdesc_at(dDSk0, ds_off);
                 if constexpr (C::kPInTmem) {
-                    // contraction step k: P^T columns 8 k, dO rows 16 k (2 KB)
-                    umma_f16_ts_x4(tm_dv, tmem + C::kColP, 8, dDOmn, 2048 >> 4, kIdPV, acc);
-                    umma_f16_ts_x4(tm_dv, tmem + C::kColP + 32, 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
+                    // contraction step k: P^T columns 8 k (from chunk 4's column on
+                    // for the second half), dO rows 16 k (2 KB)
+                    umma_f16_ts_x4(tm_dv, tmem + C::p_col(0), 8, dDOmn, 2048 >> 4, kIdPV, acc);
+                    umma_f16_ts_x4(tm_dv, tmem + C::p_col(4), 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
                 } else {
                     // P^T in shared memory: columns 16 k (32 bytes, then the next 16 KB block)
                     const uint64_t dP0 = sdesc_sw128(sbase + C::kP, 16, 1024);
@@ -1021,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                             }
                         }
                         if constexpr (C::kPInTmem) {
-                            tmem_st8(tmem + C::kColP + lane_off + sc * 8, pk);
+                            tmem_st8(tmem + C::p_col(sc) + lane_off, pk);
                         }
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
