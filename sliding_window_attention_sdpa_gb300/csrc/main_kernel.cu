@@ -83,10 +83,10 @@ struct Cfg {
     static constexpr uint32_t kV = kK + kKvStages * kTile;      // kKvStages tiles
     static constexpr uint32_t kQ = kV + kKvStages * kTile;      // kStages tiles
     static constexpr uint32_t kDO = kQ + kStages * kTile;       // kStages tiles
-    // P^T is kept in TMEM (the A operand of dV); at d = 128 a 32 KB region at kP
-    // stays for the dK/dV epilogue's staging
-    static constexpr bool kPInTmem = true;
-    static constexpr uint32_t kP = kDO + kStages * kTile;       // epilogue staging (d = 128)
+    // P^T is kept in TMEM (the A operand of dV). At d = 128 a 32 KB region at kP
+    // holds half of the dK/dV epilogue's staging (the dS^T buffer the other)
+    // and, during the dQ warps' turn, half of a stored dQ partial.
+    static constexpr uint32_t kP = kDO + kStages * kTile;
     static constexpr uint32_t kDS = kP + (HD == 64 ? 0 : 32768); // kDsBufs x dS^T [128 kv x 128 q]
     // dQ staging: 128 rows x 64 fp32 (two 16 KB blocks of 32 columns; the whole
     // row at d = 64, half of it at d = 128), or the whole 16-bit dQ tile
@@ -98,8 +98,9 @@ struct Cfg {
     static constexpr uint32_t kBytes = kMisc + 128;
     static_assert(kBytes <= 232448, "shared memory above the 227 KB a CTA may opt into");
     // The dK/dV epilogue stages two 128 x HD 16-bit tiles (2 x 16 KB at d = 64,
-    // 2 x 32 KB at d = 128) in a dS^T buffer (d = 64) or in the P^T + dS^T
-    // buffers (d = 128), all idle once the work item's contractions are done.
+    // 2 x 32 KB at d = 128) in the item's K/V ring entry (d = 64) or in the
+    // region at kP and the dS^T buffer (d = 128), all idle once the work item's
+    // contractions are done.
     static_assert(HD == 64 ? 2 * 128 * HD * 2 <= 32768 : (kDS == kP + 32768 && 2 * 128 * HD * 2 <= 65536),
                   "epilogue staging does not fit");
     // TMEM columns
@@ -120,7 +121,7 @@ struct Cfg {
     // K/V ring entry (idle once its last contractions are done), and hand the
     // entry back to the producer when their stores have read it. The softmax
     // group then runs its q-tiles back to back across items. At d = 128 the
-    // softmax group writes them, staged in its P^T and dS^T buffers.
+    // softmax group writes them, staged in the region at kP and its dS^T buffer.
     static constexpr bool kEpiDq = HD == 64;
     static_assert(!(kAhead && kDqAliasesS), "look-ahead overwrites S^T while dQ would alias it");
 };
@@ -714,18 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 // operand tiles; each contraction step adds its byte offset
                 const uint64_t dDOmn = sdesc_at(dDOmn0, q_off), dQmn = sdesc_at(dQmn0, q_off);
                 const uint64_t dDSk = sdesc_at(dDSk0, ds_off);
-                if constexpr (C::kPInTmem) {
-                    // contraction step k: P^T columns 8 k (from chunk 4's column on
-                    // for the second half), dO rows 16 k (2 KB)
-                    umma_f16_ts_x4(tm_dv, tmem + C::p_col(0), 8, dDOmn, 2048 >> 4, kIdPV, acc);
-                    umma_f16_ts_x4(tm_dv, tmem + C::p_col(4), 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
-                } else {
-                    // P^T in shared memory: columns 16 k (32 bytes, then the next 16 KB block)
-                    const uint64_t dP0 = sdesc_sw128(sbase + C::kP, 16, 1024);
-                    umma_f16_ss_x4(tm_dv, dP0, 32 >> 4, dDOmn, 2048 >> 4, kIdPV, acc);
-                    umma_f16_ss_x4(tm_dv, sdesc_at(dP0, kBlock16K), 32 >> 4, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4,
-                                   kIdPV, 1);
-                }
+                // contraction step k: P^T columns 8 k (from chunk 4's column on for
+                // the second half), dO rows 16 k (2 KB)
+                umma_f16_ts_x4(tm_dv, tmem + C::p_col(0), 8, dDOmn, 2048 >> 4, kIdPV, acc);
+                umma_f16_ts_x4(tm_dv, tmem + C::p_col(4), 8, sdesc_at(dDOmn, 4 * 2048), 2048 >> 4, kIdPV, 1);
                 // P^T is free (and, with everything issued before, the dS^T
                 // buffer of the step before this one)
                 if constexpr (C::kAhead) umma_commit(bar(kPEmpty));
@@ -1032,21 +1025,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                 tc_fence_after();
                             }
                         }
-                        if constexpr (C::kPInTmem) {
-                            tmem_st8(tmem + C::p_col(sc) + lane_off, pk);
-                        }
+                        tmem_st8(tmem + C::p_col(sc) + lane_off, pk);
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
                             const uint32_t off = swz(r, sc * 2 + m);
-                            if constexpr (!C::kPInTmem)
-                                *reinterpret_cast<uint4*>(sm + C::kP + off) =
-                                    make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                             *reinterpret_cast<uint4*>(ds_buf + off) =
                                 make_uint4(dk[4 * m], dk[4 * m + 1], dk[4 * m + 2], dk[4 * m + 3]);
                         }
                     }
                     if (!ok) break;
-                    if constexpr (C::kPInTmem) tmem_st_wait();
+                    tmem_st_wait();
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(bar(kPFull));
@@ -1082,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             named_bar_sync(kBarSoft, kSoftThreads);   // epi_slot's write is visible
             run_epi(*epi_slot);
         }
-        if constexpr (C::kPInTmem) tmem_st_wait();   // a step left early may have P^T stores in flight
+        tmem_st_wait();   // a step left early may have P^T stores in flight
     } else {
         if constexpr (C::kAhead) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;");
         // ------------------------------------------------------------ dQ
@@ -1554,10 +1542,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     if (conv_now && use_tma && go && !single && k + 1 < it.steps) {
                         // Adds the stored partial and converts, a 64-column half at a
                         // time: the fp32 partial comes by TMA (half 0 into the staging,
-                        // half 1 into the P^T buffer, idle from the dQ contraction to
-                        // this group's release; an item's last step leaves it to the
-                        // dK/dV epilogue), this visit's dQ from TMEM, and each half of
-                        // the 16-bit tile goes out from the staging.
+                        // half 1 into the epilogue's region at kP, idle apart from an
+                        // item's last step, which this path leaves out), this visit's
+                        // dQ from TMEM, and each half of the 16-bit tile goes out from
+                        // the staging.
                         uint32_t ld0 = pre_ld;
                         if (!pre0) {
                             ld0 = ld_it++;
@@ -1608,7 +1596,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                                 }
                             }
                             if (hf == 1) {
-                                // TMEM and the P^T buffer have been read
+                                // TMEM and the region at kP have been read
                                 tc_fence_before();
                                 mbar_arrive(bar(kDqEmpty));
                             }
