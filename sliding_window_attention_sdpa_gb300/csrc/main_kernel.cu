@@ -399,15 +399,52 @@ struct Walk {
     int64_t begin, end, stride;
 };
 
+// Strip mode with sequences of different lengths (packed, or length arrays):
+// the offset, inside a group's items, of run boundary `run` of `runs`, placed
+// so that each run holds an equal share of the kv-tiles that hold keys
+// (ceil(len_kv / 128) per sequence and kv-head). Items past a sequence's keys
+// (slot padding, dK/dV zero-fill only) go with the run before them. With
+// equal shares of items instead, a run over long sequences held all their
+// work and one over short ones little. -1 if no sequence holds keys.
+__device__ __forceinline__ int64_t work_boundary(const Geometry& g, int64_t n_kv_tiles, int64_t group_heads,
+                                                 int64_t run, int64_t runs)
+{
+    auto tiles = [&](int64_t bi) -> int64_t {
+        const int64_t t = (seq_info(g, bi).len_kv + kTileKV - 1) / kTileKV;
+        return t < n_kv_tiles ? t : n_kv_tiles;
+    };
+    int64_t per_head = 0;
+    for (int64_t bi = 0; bi < g.b; ++bi) per_head += tiles(bi);
+    if (per_head == 0) return -1;
+    const int64_t total = per_head * group_heads;
+    if (run <= 0) return 0;
+    if (run >= runs) return group_heads * g.b * n_kv_tiles;
+    const int64_t target = total * run / runs;   // working tiles before the boundary
+    const int64_t head = target / per_head;
+    int64_t rem = target - head * per_head;
+    for (int64_t bi = 0; bi < g.b; ++bi) {
+        const int64_t t = tiles(bi);
+        if (rem < t) return (head * g.b + bi) * n_kv_tiles + rem;
+        rem -= t;
+    }
+    return (head + 1) * g.b * n_kv_tiles;   // not reached
+}
+
 template <bool STRIP>
-__device__ __forceinline__ Walk item_walk(int64_t n_items, int64_t h_kv, int64_t group_heads)
+__device__ __forceinline__ Walk item_walk(const Geometry& g, int64_t n_items, int64_t n_kv_tiles, int64_t group_heads)
 {
     if constexpr (STRIP) {
         // groups of group_heads consecutive kv-heads share R runs: CTA c walks
         // group c % (h_kv / group_heads) over the (c / ...)-th run of its items
-        const int64_t n_groups = h_kv / group_heads;
+        const int64_t n_groups = g.h_kv / group_heads;
         const int64_t runs = gridDim.x / n_groups, grp = blockIdx.x % n_groups, run = blockIdx.x / n_groups;
-        const int64_t per_group = n_items / h_kv * group_heads;
+        const int64_t per_group = n_items / g.h_kv * group_heads;
+        if ((g.layout == 1 || g.seq_kv_lens != nullptr) && g.b <= 256) {
+            const int64_t lo = work_boundary(g, n_kv_tiles, group_heads, run, runs);
+            if (lo >= 0)
+                return Walk{grp * per_group + lo, grp * per_group + work_boundary(g, n_kv_tiles, group_heads,
+                                                                                  run + 1, runs), 1};
+        }
         return Walk{grp * per_group + per_group * run / runs, grp * per_group + per_group * (run + 1) / runs, 1};
     }
     return Walk{static_cast<int64_t>(blockIdx.x), n_items, static_cast<int64_t>(gridDim.x)};
@@ -534,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const bool thd = g.layout == 1;
     const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
                          static_cast<uint32_t>(g.h_q / g.h_kv), static_cast<uint32_t>(g.b)};
-    const Walk wk = item_walk<STRIP>(n_items, g.h_kv, a.strip > 0 ? a.strip : 1);
+    const Walk wk = item_walk<STRIP>(g, n_items, a.n_kv_tiles, a.strip > 0 ? a.strip : 1);
 
     if (tid == 0) {
         misc[1] = 0;
