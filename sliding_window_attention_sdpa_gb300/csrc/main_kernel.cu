@@ -387,7 +387,8 @@ struct ItemCounts {
 //  - Strip mode: items numbered (kv-head, sequence, kv-tile), kv-tile
 //    fastest. Groups of G consecutive kv-heads (G chosen by the launcher so
 //    that the grid fills the SMs: 16 kv-heads on 152 SMs take G = 2, 19 runs
-//    per group) share R equal contiguous runs of their items; CTA c walks
+//    per group) share R contiguous runs of their items, equal in items, or
+//    (sequences of different lengths) in kv-tiles that hold keys; CTA c walks
 //    group c % (h_kv / G) over run c / (h_kv / G). The two kv-tiles visiting
 //    a q-tile are then consecutive items of one CTA except where a run ends.
 //    A run may cross from one kv-head or sequence into the next: no q-tile
@@ -1256,17 +1257,17 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 const bool use_tma = !thd || (j + 1) * kTileQ <= it.s.slot_q;
                 // Strip mode (at most two visitors, kv-tiles t and t + 1 of one
                 // head): the two are consecutive items of this CTA unless its run
-                // ends between them ("local"), and combine with no waiting. With
-                // one q-head per kv-head their dQ contractions add up in tensor
-                // memory; otherwise the first stores its fp32 partial in the
-                // accumulator rows and the second loads it back. A pair split
+                // ends between them ("local"), and combine with no waiting. At
+                // d = 64 with one q-head per kv-head their dQ contractions add up
+                // in tensor memory; otherwise the first stores its fp32 partial in
+                // the accumulator rows and the second loads it back. A pair split
                 // between two CTAs goes by arrival order: the first to arrive
                 // stores its partial and flags it, the second adds it to its own.
                 // A sum of two rounded partials does not depend on their order,
                 // so this stays bitwise repeatable.
                 const bool local = STRIP && nvis == 2 && (turn == 0 ? item + 1 < wk.end : item > wk.begin);
-                // one q-head per kv-head: the pair's dQ adds up in tensor memory
-                // (tmem_pair); the first step reads nothing, the second the sum
+                // d = 64, one q-head per kv-head: the pair's dQ adds up in tensor
+                // memory (tmem_pair); the first step reads nothing, the second the sum
                 const int tpair = kTmemPairs && local && it.group == 1 ? 1 + turn : 0;
                 if (tpair == 1) continue;
                 const bool pair = STRIP && nvis == 2 && !local;
@@ -1573,9 +1574,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 } else {
                     go = wait_turn();
                     if (r == 0) SWA_TRACE(15, dq_it - 1);
-                    // With a partial sum to add, the row-wise path loads it eight
-                    // rows at a time; read per row here, its latency would hold
-                    // the dQ columns of TMEM (aliasing S^T) four times over.
+                    // A partial sum to add comes by TMA for whole tiles (first
+                    // branch); tiles that end past a THD slot take the row-wise
+                    // path, which loads it eight rows at a time (read per row, its
+                    // latency would hold the dQ columns of TMEM, aliasing S^T, four
+                    // times over).
                     if (conv_now && use_tma && go && !single && k + 1 < it.steps) {
                         // Adds the stored partial and converts, a 64-column half at a
                         // time: the fp32 partial comes by TMA (half 0 into the staging,
@@ -1779,7 +1782,7 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
         // more kv-heads than SMs).
         const int64_t per_head = items / a.g.h_kv;
         int64_t best = 0;
-        for (int64_t G = 1; G <= a.g.h_kv && G <= 8; G *= 2) {
+        for (int64_t G = 1; G <= a.g.h_kv && G <= 8; ++G) {   // e.g. 6 kv-heads: G = 3, 2 x 76 runs
             if (a.g.h_kv % G) continue;
             int64_t runs = sms * G / a.g.h_kv;
             if (runs > per_head * G) runs = per_head * G;
