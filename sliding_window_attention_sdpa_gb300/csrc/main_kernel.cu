@@ -334,15 +334,27 @@ struct Item {
     // that can pair when a q-tile has at most two visitors), set by with_pairs
     uint8_t tp_first, tp_last;
     // Steps run q-head h0 .. h0 + group - 1, each over its q-tiles from q_hi - 1
-    // down to q_lo, or (strip mode, UP) from q_lo up to q_hi - 1; counters
-    // rather than divisions (there is no 64-bit divider, and these sit on every
-    // role's hand-off path).
+    // down to q_lo, or (strip mode, UP) from q_lo up to q_hi - 1. With QMAJOR
+    // (strip mode at d = 64) they run q-tile by q-tile instead, each over every
+    // q-head of the group, so that the q-tile this item shares with the next
+    // one (its Q and dO rows, and the partial dQ the pair passes on) comes back
+    // to the CTA after one q-tile's steps, not a whole item's. (At d = 128 that
+    // order bunches the steps that add a partial, whose dQ turn holds S^T's
+    // columns, and was slower.) Counters rather than divisions (there is no
+    // 64-bit divider, and these sit on every role's hand-off path).
     template <bool UP>
     __device__ __forceinline__ int64_t first_j() const { return UP ? q_lo : q_hi - 1; }
-    template <bool UP>
+    template <bool UP, bool QMAJOR = false>
     __device__ __forceinline__ void advance(int64_t& j, int64_t& hh) const
     {
-        if constexpr (UP) {
+        if constexpr (UP && QMAJOR) {
+            if (hh == h0 + group - 1) {
+                hh = h0;
+                ++j;
+            } else {
+                ++hh;
+            }
+        } else if constexpr (UP) {
             if (j == q_hi - 1) {
                 j = q_lo;
                 ++hh;
@@ -615,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     // which the next step overwrites, so the pair goes through the
     // accumulator rows instead.
     constexpr bool kTmemPairs = STRIP && !C::kDqAliasesS;
+    constexpr bool kQMajor = STRIP && !C::kDqAliasesS;   // the step order within an item (Item::advance)
     if (use_items)
         for (int64_t item = wk.begin + static_cast<int64_t>(tid) * wk.stride; item < wk.end;
              item += static_cast<int64_t>(kThreads) * wk.stride)
@@ -684,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 tma_tile<HD>(sbase + C::kV + ks * C::kTile, &a.tm_v, bar(kKvFull0 + ks), thd,
                              (int)it.gk, kvrow, (int)it.bi);
                 bool ok = true;
-                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
+                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP, kQMajor>(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (!wait(kQEmpty0 + st, ((q_it / C::kStages) & 1) ^ 1)) { ok = false; break; }
                     SWA_TRACE(12, q_it);
@@ -811,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             ++kv_it;
             if (it.kv_base + kTileKV > it.s.len_kv)
                 zero_tail<HD>(sm + C::kK + ks * C::kTile, it.s.len_kv - it.kv_base, lane);
-            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
+            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP, kQMajor>(j, hh)) {
                 const int st = q_it % C::kStages;
                 if (!(ok = wait_warp(kQFull0 + st, (q_it / C::kStages) & 1))) break;
                 if (lane == 0) SWA_TRACE(0, q_it);
@@ -983,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                 if (g.right >= 0) i_lo = imax(i_lo, kj - g.right - it.s.diag);
                 if (g.window_left >= 0) i_hi = imin(i_hi, kj + g.window_left - it.s.diag);
                 if (kj >= it.s.len_kv) i_hi = -1;
-                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP>(j, hh)) {
+                for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, ++q_it, it.template advance<STRIP, kQMajor>(j, hh)) {
                     const int st = q_it % C::kStages;
                     if (lane == 0 && warp == kWarpSoft0) SWA_TRACE(20, q_it);
                     if constexpr (!C::kEpiDq)
@@ -1244,7 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
             }
             const int eks = static_cast<int>(ekv_it % C::kKvStages);
             const uint32_t epar = eacc_it & 1;
-            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, it.template advance<STRIP>(j, hh)) {
+            for (int64_t k = 0, j = it.first_j<STRIP>(), hh = it.h0; k < it.steps; ++k, it.template advance<STRIP, kQMajor>(j, hh)) {
                 // this visit's bookkeeping first, while the dQ contraction runs
                 // (after the wait it delayed the TMEM read by ~1 K cycles)
                 int64_t first, nvis;
@@ -1298,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
                     Item nx = it;
                     bool have = true;
                     if (k + 1 < it.steps) {
-                        it.template advance<STRIP>(j2, h2);
+                        it.template advance<STRIP, kQMajor>(j2, h2);
                     } else if (item + wk.stride < wk.end) {
                         nx = item_at(item + wk.stride);
                         j2 = nx.first_j<STRIP>();
