@@ -269,7 +269,7 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "696fc55a2edbbab9", "bytes": 283118336},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "c59f6f3e398a84ac", "bytes": 283210496},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).
