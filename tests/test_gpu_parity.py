@@ -86,6 +86,10 @@ SMALL = [
          thd_lens=[390, 64, 1000, 129], slot_align=8, seed=31),
     Case("thd_strip_d128_mha_40seq_w128_rowwise_det", 0, 1, 1, 0, 0, 128, "tl", 128, layout="thd",
          thd_lens=[300 + (37 * i) % 300 for i in range(40)], slot_align=8, det=True, seed=32),
+    # strip runs split by kv-tiles that hold keys, with empty sequences first
+    # and in between, and more runs (76 per kv-head) than such kv-tiles (18)
+    Case("thd_strip_runs_by_work_leading_empty_det", 0, 4, 2, 0, 0, 64, "tl", 128, layout="thd",
+         thd_lens=[0, 0, 700, 0, 64, 1300, 0], slot_align=8, det=True, seed=33),
 ]
 
 
