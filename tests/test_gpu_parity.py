@@ -263,3 +263,17 @@ def test_thd_varlen_sinks_det_full_size_bitwise_repeatable():
     check_all(bt, out)
     del bt, out
     torch.cuda.empty_cache()
+
+
+def test_full_size_d128_deterministic_is_bitwise_repeatable():
+    """Deterministic mode at b12 h48/6 d128 S16484 bottom-right W96 (strip
+    mode at d = 128: pairs through the accumulator rows, the partial loaded by
+    TMA): three passes give the same bits, and a sampled unit matches the
+    oracle."""
+    case = Case("gqa_b12_h48x6_d128_s16484_br_w96_det3", 12, 48, 6, 16484, 16484, 128, "br", 96,
+                det=True, seed=1012, gen_device="cuda")
+    bt = build(case, units=[(5, 4)])
+    out = _three_runs_bitwise(bt)
+    check_all(bt, out)
+    del bt, out
+    torch.cuda.empty_cache()
