@@ -21,6 +21,9 @@ dirty line of the flush is left for the step's first kernel to write back
   roofline   the main kernel: algorithmic bytes per launch / its mean duration
              (CUDA events on the launching stream) against measured HBM peak
   cpu_baseline  the fp64 CPU oracle on the same workload (host cores)
+  other_workloads  (one GPU, default workload) the benchmark set's other
+             shapes, each timed the same way after the headline's figures:
+             whole step and main kernel, CUDA events, L2 flushed
 
 --impl reference times that oracle as the reference arm (no GPU work).
 Multi-GPU (torchrun): every rank runs an independent replica (weak scaling).
@@ -67,6 +70,19 @@ THD_WORKLOADS = {
                                              w=128, dtype="f16", sink=True, det=True, seed=1005, align=128),
 }
 DEFAULT = "gptoss_b2_h16_d64_w128_s8192"
+# The benchmark set's other shapes (workload, deterministic), timed after the
+# default workload's figures by a one-GPU run of the default workload.
+OTHER_WORKLOADS = (
+    ("gptoss_b2_h16_d64_w128_s8192", True),
+    ("gptoss_b2_h16_d64_w128_s2048", False),
+    ("gptoss_b2_h16_d64_w128_s4096", False),
+    ("gptoss_b2_h16_d64_w128_s32768", False),
+    ("gqa_b12_h48x6_d128_s16484_br_w96", False),
+    ("gqa_b24_h28x4_d128_s128_br_w8000", False),
+    ("nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000", False),
+    ("winonly_b4_h16_d64_s4096_w512", False),
+    ("thd16_h64x8_d64_f16_w128_sink_det", True),
+)
 MODE = {"none": 0, "tl": 1, "br": 2}
 L2_FLUSH_BYTES = 512 << 20
 
@@ -215,12 +231,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, log_dir: str | None = None):
+    def __init__(self, gpu_index: int, log_dir: str | None = None, tag: str = ""):
         import tempfile
         self.gpu = gpu_index
         self.proc = None
         # the raw samples; the JSON line carries their summary
-        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}{tag}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -333,6 +349,32 @@ def time_device(prob: Problem, steps: int, warmup: int):
     torch.cuda.synchronize()
     main = [a.elapsed_time(b) for a, b in ev]
     return total, main
+
+
+def time_other_workloads(device, steps: int, warmup: int, peak_gbs: float, peak_tf: float):
+    """Whole-step and main-kernel device times of OTHER_WORKLOADS, one shape
+    at a time (its tensors freed before the next). A shape that fails to run
+    is reported with its error instead of stopping the benchmark."""
+    out = []
+    for name, det in OTHER_WORKLOADS:
+        rec = {"workload": name, "deterministic": det}
+        try:
+            prob = Problem(name, device, seed=1000 + 2, deterministic=det)
+            total, main = time_device(prob, steps, warmup)
+            status = prob.swa.sdpa_bwd_check_status(prob.ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+            step_ms, main_ms = statistics.median(total), statistics.median(main)
+            rec.update(step_ms=step_ms, main_kernel_ms=main_ms,
+                       step_tflops=prob.flops / (step_ms * 1e-3) / 1e12,
+                       main_kernel_tflops=prob.flops / (main_ms * 1e-3) / 1e12,
+                       tensor_peak_frac=prob.flops / (main_ms * 1e-3) / 1e12 / peak_tf,
+                       hbm_frac=prob.main_bytes / (main_ms * 1e-3) / 1e9 / peak_gbs,
+                       device_status=int(status))
+            del prob
+        except Exception as e:  # noqa: BLE001 - reported in the line, not fatal
+            rec["error"] = f"{type(e).__name__}: {e}"[:300]
+        torch.cuda.empty_cache()
+        out.append(rec)
+    return out
 
 
 def time_forward(prob: Problem, steps: int, warmup: int):
@@ -574,6 +616,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(THD_WORKLOADS))
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the benchmark set's other shapes after the default workload")
     ap.add_argument("--clock-log-dir", default=None,
                     help="folder for the raw nvidia-smi clock samples (default: the temp folder)")
     args = ap.parse_args()
@@ -655,12 +699,22 @@ def main():
                     "traffic": measured_traffic(args.workload, FWD_TRAFFIC, FWD_SOURCES),
                     "device_status": int(fwd_status)},
     }
+    flops = prob.flops
+    if world == 1 and args.workload == DEFAULT and not args.no_other_workloads:
+        del prob   # the other shapes get the device memory to themselves
+        torch.cuda.empty_cache()
+        with ClockSampler(local, args.clock_log_dir, tag="_other") as clk_other:
+            others = time_other_workloads(dev, min(args.steps, 10), 3, peak_gbs, peak_tf)
+        line["other_workloads"] = {
+            "steps": min(args.steps, 10), "warmup": 3, "stat": "median",
+            "l2": "flushed between timed steps, as for the default workload",
+            "clocks": clk_other.summary(), "results": others}
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         name = args.workload
         units = cpu_units_for_budget(name, 15.0, cores)
         sec, frac = cpu_oracle_step(name, cores, units)
-        cpu_val = prob.flops * frac / sec / 1e12
+        cpu_val = flops * frac / sec / 1e12
         sp = spec(name)
         line["cpu_baseline"] = {"value": cpu_val, "unit": "TFLOP/s", "cores": cores,
                                 "kind": "oracle",

@@ -59,3 +59,17 @@ def test_two_rank_max_and_aggregate():
         assert step == 3.0 and e2e == 7.0
         # 2 ranks x 1 TFLOP over the slowest rank's 3 ms
         assert abs(value - 2.0 / 3e-3) < 1e-9
+
+
+def test_other_workloads_are_known_shapes():
+    """Every shape timed after the default workload is one of the benchmark
+    set's workloads, none twice, and the default appears only in its
+    deterministic mode (its non-deterministic figures are the line's own)."""
+    names = [(n, det) for n, det in bench.OTHER_WORKLOADS]
+    assert len(set(names)) == len(names)
+    for n, det in names:
+        assert n in bench.WORKLOADS or n in bench.THD_WORKLOADS
+        assert n != bench.DEFAULT or det
+        # spec() resolves each (THD lengths included) without a device
+        sp = bench.spec(n)
+        assert bench.workload_flops(sp) > 0
