@@ -78,9 +78,12 @@ OTHER_WORKLOADS = (
     ("gptoss_b2_h16_d64_w128_s4096", False),
     ("gptoss_b2_h16_d64_w128_s32768", False),
     ("gqa_b12_h48x6_d128_s16484_br_w96", False),
+    ("gqa_b12_h48x6_d128_s16484_br_w96", True),
     ("gqa_b24_h28x4_d128_s128_br_w8000", False),
     ("nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000", False),
+    ("nonsquare_b12_h40x8_d64_q128_kv8960_br_w8000", True),
     ("winonly_b4_h16_d64_s4096_w512", False),
+    ("winonly_b4_h16_d64_s4096_w512", True),
     ("thd16_h64x8_d64_f16_w128_sink_det", True),
 )
 MODE = {"none": 0, "tl": 1, "br": 2}
