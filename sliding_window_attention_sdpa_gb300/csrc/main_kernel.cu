@@ -46,6 +46,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <type_traits>
+#include <vector>
+
 #include "ptx.cuh"
 #include "sdpa_internal.h"
 #include "seq.cuh"
@@ -412,6 +416,21 @@ struct Walk {
     int64_t begin, end, stride;
 };
 
+// The round-robin walk's item order, set by the host when it knows every item's
+// steps (BSHD, no length arrays): items go out longest first, each to the CTA
+// with the fewest steps so far, and each CTA takes its own in ascending number,
+// so that a relay partner (the kv-tile before, a lower number) is never behind
+// the item that waits for it. n = 0: CTA c takes c, c + grid, ...
+constexpr int kOrderMaxItems = 4096, kOrderMaxCtas = 256;
+struct ItemOrder {
+    int32_t n;                            // items listed, 0 for none
+    uint16_t off[kOrderMaxCtas + 1];      // CTA c takes item[off[c]] .. item[off[c + 1] - 1]
+    uint16_t item[kOrderMaxItems];
+};
+struct NoOrder {
+    int32_t n;
+};
+
 // Strip mode with sequences of different lengths (packed, or length arrays):
 // the offset, inside a group's items, of run boundary `run` of `runs`, placed
 // so that each run holds an equal share of the kv-tiles that hold keys
@@ -547,6 +566,11 @@ __device__ __forceinline__ void zero_tail(uint8_t* tile, int64_t nvalid, int lan
 
 }  // namespace
 
+__device__ __forceinline__ int64_t ord_off(const ItemOrder& o, unsigned c) { return o.off[c]; }
+__device__ __forceinline__ int64_t ord_off(const NoOrder&, unsigned) { return 0; }
+__device__ __forceinline__ int64_t ord_item(const ItemOrder& o, int64_t i) { return o.n > 0 ? o.item[i] : i; }
+__device__ __forceinline__ int64_t ord_item(const NoOrder&, int64_t i) { return i; }
+
 // A global-memory wait (relay turn, split pair) that ran out: marks the CTA
 // aborted and records the status and which wait it was (out of line: cold).
 __device__ __noinline__ bool gave_up(int32_t* status, volatile uint32_t* abort_flag, int where)
@@ -558,7 +582,9 @@ __device__ __noinline__ bool gave_up(int32_t* status, volatile uint32_t* abort_f
 }
 
 template <int HD, bool BF16, bool STRIP>
-__global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a)
+__global__ void __launch_bounds__(kThreads, 1)
+    sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a,
+                         const __grid_constant__ std::conditional_t<STRIP, NoOrder, ItemOrder> ord)
 {
     using C = Cfg<HD>;
     // The 128-byte-swizzled operand tiles need a 1024-byte aligned base; the
@@ -584,7 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     const bool thd = g.layout == 1;
     const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
                          static_cast<uint32_t>(g.h_q / g.h_kv), static_cast<uint32_t>(g.b)};
-    const Walk wk = item_walk<STRIP>(g, n_items, a.n_kv_tiles, a.strip > 0 ? a.strip : 1);
+    const Walk wk = !STRIP && ord.n > 0 ? Walk{ord_off(ord, blockIdx.x), ord_off(ord, blockIdx.x + 1), 1}
+                                        : item_walk<STRIP>(g, n_items, a.n_kv_tiles, a.strip > 0 ? a.strip : 1);
+    // item number at walk position i (the same unless the host set an order)
+    auto item_no = [&](int64_t i) -> int64_t { return ord_item(ord, i); };
 
     if (tid == 0) {
         misc[1] = 0;
@@ -631,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     if (use_items)
         for (int64_t item = wk.begin + static_cast<int64_t>(tid) * wk.stride; item < wk.end;
              item += static_cast<int64_t>(kThreads) * wk.stride)
-            items[item] = with_pairs<kTmemPairs>(g, decode<STRIP>(a, cnt, item), item, wk);
-    auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode<STRIP>(a, cnt, i); };
+            items[item] = with_pairs<kTmemPairs>(g, decode<STRIP>(a, cnt, item_no(item)), item, wk);
+    auto item_at = [&](int64_t i) -> Item { return use_items ? items[i] : decode<STRIP>(a, cnt, item_no(i)); };
     tc_fence_before();
     __syncthreads();   // also publishes the item table to the CTA
     tc_fence_after();
@@ -1774,6 +1803,55 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_main_kernel(const __grid
     }
 }
 
+// The round-robin walk's order (ItemOrder) for BSHD problems without length
+// arrays: every item of kv-tile t takes the same steps, (q-tiles it sweeps) x
+// (q-heads per kv-head), plus one for its dK/dV store. False (plain round
+// robin) when the host cannot tell the steps or the table does not hold them.
+static bool balanced_order(const MainArgs& a, int64_t items, int64_t grid, ItemOrder& o)
+{
+    o.n = 0;
+    const Geometry& g = a.g;
+    if (g.layout != 0 || g.seq_q_lens || g.seq_kv_lens || items > kOrderMaxItems || grid > kOrderMaxCtas ||
+        grid < 2)
+        return false;
+    SeqInfo sq{};
+    sq.slot_q = sq.len_q = g.s_q;
+    sq.slot_kv = sq.len_kv = g.s_kv;
+    sq.diag = g.mask_mode == 2 ? g.s_kv - g.s_q : 0;
+    const int64_t group = g.h_q / g.h_kv;
+    std::vector<int64_t> steps(a.n_kv_tiles);
+    for (int64_t t = 0; t < a.n_kv_tiles; ++t) {
+        int64_t lo, hi;
+        q_tile_range(g, sq, t, lo, hi);
+        steps[t] = (hi > lo ? hi - lo : 0) * group + 1;
+    }
+    // items numbered head fastest: kv-tile (i / h_kv) mod n_kv_tiles
+    auto work = [&](int64_t i) { return steps[(i / g.h_kv) % a.n_kv_tiles]; };
+    std::vector<int32_t> by_work(items);
+    for (int64_t i = 0; i < items; ++i) by_work[i] = static_cast<int32_t>(i);
+    std::stable_sort(by_work.begin(), by_work.end(), [&](int32_t x, int32_t y) { return work(x) > work(y); });
+    // longest first to the least-loaded CTA (ties: the lower CTA)
+    std::vector<std::pair<int64_t, int32_t>> heap;
+    for (int32_t c = 0; c < grid; ++c) heap.push_back({0, c});
+    auto later = [](const std::pair<int64_t, int32_t>& x, const std::pair<int64_t, int32_t>& y) { return x > y; };
+    std::vector<int32_t> cta_of(items);
+    for (int32_t i : by_work) {
+        std::pop_heap(heap.begin(), heap.end(), later);
+        cta_of[i] = heap.back().second;
+        heap.back().first += work(i);
+        std::push_heap(heap.begin(), heap.end(), later);
+    }
+    // each CTA's items in ascending number
+    std::vector<int32_t> count(grid + 1, 0);
+    for (int64_t i = 0; i < items; ++i) ++count[cta_of[i] + 1];
+    for (int64_t c = 0; c < grid; ++c) count[c + 1] += count[c];
+    for (int64_t c = 0; c <= grid; ++c) o.off[c] = static_cast<uint16_t>(count[c]);
+    std::vector<int32_t> fill(count.begin(), count.end() - 1);
+    for (int64_t i = 0; i < items; ++i) o.item[fill[cta_of[i]]++] = static_cast<uint16_t>(i);
+    o.n = static_cast<int32_t>(items);
+    return true;
+}
+
 template <int HD, bool BF16, bool STRIP>
 static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 {
@@ -1824,7 +1902,16 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = STRIP ? 1 : 0;
-    if ((e = cudaLaunchKernelEx(&cfg, kern, b)) != cudaSuccess) return e;
+    if constexpr (STRIP) {
+        const NoOrder ord{0};
+        if ((e = cudaLaunchKernelEx(&cfg, kern, b, ord)) != cudaSuccess) return e;
+    } else {
+        static_assert(kOrderMaxItems <= 65536, "item numbers are 16-bit");
+        // built per launch on the host; passed by value with the launch
+        static thread_local ItemOrder ord;
+        balanced_order(b, items, grid, ord);
+        if ((e = cudaLaunchKernelEx(&cfg, kern, b, ord)) != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
