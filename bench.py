@@ -288,7 +288,7 @@ class ClockSampler:
 # for the kernel source it was taken on (sha256 of the main kernel's sources,
 # first 16 hex digits); any other source reports null.
 MAIN_TRAFFIC = {
-    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "c59f6f3e398a84ac", "bytes": 283210496},
+    "gptoss_b2_h16_d64_w128_s8192": {"kernel": "2b44da694746a8eb", "bytes": 283117056},
 }
 KERNEL_SOURCES = ("main_kernel.cu", "ptx.cuh", "seq.cuh", "sdpa_internal.h")
 # The same for one forward launch (profiles/sdpa_fwd_kernel_*.md).

@@ -420,16 +420,14 @@ struct Walk {
 // steps (BSHD, no length arrays): items go out longest first, each to the CTA
 // with the fewest steps so far, and each CTA takes its own in ascending number,
 // so that a relay partner (the kv-tile before, a lower number) is never behind
-// the item that waits for it. n = 0: CTA c takes c, c + grid, ...
+// the item that waits for it. Without one (NoOrder, the kernel instance
+// whose parameter it is), CTA c takes c, c + grid, ...
 constexpr int kOrderMaxItems = 4096, kOrderMaxCtas = 256;
 struct ItemOrder {
-    int32_t n;                            // items listed, 0 for none
     uint16_t off[kOrderMaxCtas + 1];      // CTA c takes item[off[c]] .. item[off[c + 1] - 1]
     uint16_t item[kOrderMaxItems];
 };
-struct NoOrder {
-    int32_t n;
-};
+struct NoOrder {};
 
 // Strip mode with sequences of different lengths (packed, or length arrays):
 // the offset, inside a group's items, of run boundary `run` of `runs`, placed
@@ -568,7 +566,7 @@ __device__ __forceinline__ void zero_tail(uint8_t* tile, int64_t nvalid, int lan
 
 __device__ __forceinline__ int64_t ord_off(const ItemOrder& o, unsigned c) { return o.off[c]; }
 __device__ __forceinline__ int64_t ord_off(const NoOrder&, unsigned) { return 0; }
-__device__ __forceinline__ int64_t ord_item(const ItemOrder& o, int64_t i) { return o.n > 0 ? o.item[i] : i; }
+__device__ __forceinline__ int64_t ord_item(const ItemOrder& o, int64_t i) { return o.item[i]; }
 __device__ __forceinline__ int64_t ord_item(const NoOrder&, int64_t i) { return i; }
 
 // A global-memory wait (relay turn, split pair) that ran out: marks the CTA
@@ -581,11 +579,12 @@ __device__ __noinline__ bool gave_up(int32_t* status, volatile uint32_t* abort_f
     return false;
 }
 
-template <int HD, bool BF16, bool STRIP>
+template <int HD, bool BF16, bool STRIP, bool ORDER>
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_bwd_main_kernel(const __grid_constant__ MainArgs a,
-                         const __grid_constant__ std::conditional_t<STRIP, NoOrder, ItemOrder> ord)
+                         const __grid_constant__ std::conditional_t<ORDER, ItemOrder, NoOrder> ord)
 {
+    static_assert(!(STRIP && ORDER), "the strip walk sets its own order");
     using C = Cfg<HD>;
     // The 128-byte-swizzled operand tiles need a 1024-byte aligned base; the
     // dynamic shared memory is declared so, and checked rather than padded
@@ -610,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool thd = g.layout == 1;
     const ItemCounts cnt{static_cast<uint32_t>(g.h_kv), static_cast<uint32_t>(a.n_kv_tiles),
                          static_cast<uint32_t>(g.h_q / g.h_kv), static_cast<uint32_t>(g.b)};
-    const Walk wk = !STRIP && ord.n > 0 ? Walk{ord_off(ord, blockIdx.x), ord_off(ord, blockIdx.x + 1), 1}
-                                        : item_walk<STRIP>(g, n_items, a.n_kv_tiles, a.strip > 0 ? a.strip : 1);
+    const Walk wk = ORDER ? Walk{ord_off(ord, blockIdx.x), ord_off(ord, blockIdx.x + 1), 1}
+                          : item_walk<STRIP>(g, n_items, a.n_kv_tiles, a.strip > 0 ? a.strip : 1);
     // item number at walk position i (the same unless the host set an order)
     auto item_no = [&](int64_t i) -> int64_t { return ord_item(ord, i); };
 
@@ -1809,7 +1808,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // robin) when the host cannot tell the steps or the table does not hold them.
 static bool balanced_order(const MainArgs& a, int64_t items, int64_t grid, ItemOrder& o)
 {
-    o.n = 0;
     const Geometry& g = a.g;
     if (g.layout != 0 || g.seq_q_lens || g.seq_kv_lens || items > kOrderMaxItems || grid > kOrderMaxCtas ||
         grid < 2)
@@ -1848,17 +1846,14 @@ static bool balanced_order(const MainArgs& a, int64_t items, int64_t grid, ItemO
     for (int64_t c = 0; c <= grid; ++c) o.off[c] = static_cast<uint16_t>(count[c]);
     std::vector<int32_t> fill(count.begin(), count.end() - 1);
     for (int64_t i = 0; i < items; ++i) o.item[fill[cta_of[i]]++] = static_cast<uint16_t>(i);
-    o.n = static_cast<int32_t>(items);
     return true;
 }
 
 template <int HD, bool BF16, bool STRIP>
 static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
 {
-    auto kern = sdpa_bwd_main_kernel<HD, BF16, STRIP>;
     const uint32_t bytes = Cfg<HD>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     const int64_t items = a.g.b * a.g.h_kv * a.n_kv_tiles;
     if (items == 0) return cudaSuccess;
     int dev = 0, sms = 0;
@@ -1902,15 +1897,21 @@ static cudaError_t launch_typed(const MainArgs& a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = STRIP ? 1 : 0;
-    if constexpr (STRIP) {
-        const NoOrder ord{0};
+    static_assert(kOrderMaxItems <= 65536, "item numbers are 16-bit");
+    // the balanced order, built per launch on the host and passed by value
+    // with it (its own kernel instance, so that launches without one carry no
+    // order parameter)
+    static thread_local ItemOrder ord;
+    if (!STRIP && balanced_order(b, items, grid, ord)) {
+        auto kern = sdpa_bwd_main_kernel<HD, BF16, false, true>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+            return e;
         if ((e = cudaLaunchKernelEx(&cfg, kern, b, ord)) != cudaSuccess) return e;
     } else {
-        static_assert(kOrderMaxItems <= 65536, "item numbers are 16-bit");
-        // built per launch on the host; passed by value with the launch
-        static thread_local ItemOrder ord;
-        balanced_order(b, items, grid, ord);
-        if ((e = cudaLaunchKernelEx(&cfg, kern, b, ord)) != cudaSuccess) return e;
+        auto kern = sdpa_bwd_main_kernel<HD, BF16, STRIP, false>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+            return e;
+        if ((e = cudaLaunchKernelEx(&cfg, kern, b, NoOrder{})) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
